@@ -1,0 +1,297 @@
+"""CPU oracle for block-scaled 4-bit quantisation -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package.  The product library never
+imports it; it shares no code with the CUDA path.
+
+The arithmetic lives in ``nvq_oracle.c`` (plain C, one thread, binary32 with
+contraction off).  This module compiles it with gcc and wraps it for numpy
+arrays.  Every function cites the source passage it restates in the C file.
+
+Parity status: all functions are pinned by host tests; the NF4 level table is
+"parity unpinned" against third-party tables (it is derived here from the
+published normal-quantile construction).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvq_oracle.c")
+_LIB = os.path.join(_HERE, "libnvq_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FLAG_4OVER6 = 1
+FLAG_AMAX_GIVEN = 2
+STATUS_NONFINITE = 1
+STATUS_BAD_INDEX = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, no fast math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+               "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = C.CDLL(_LIB)
+            P = C.c_void_p
+            i64 = C.c_int64
+            u32 = C.c_uint32
+            lib.oracle_bf16_to_f32.restype = C.c_float
+            lib.oracle_bf16_to_f32.argtypes = [C.c_uint16]
+            lib.oracle_f32_to_bf16.restype = C.c_uint16
+            lib.oracle_f32_to_bf16.argtypes = [C.c_float]
+            lib.oracle_e4m3_value.restype = C.c_float
+            lib.oracle_e4m3_value.argtypes = [C.c_uint8]
+            lib.oracle_e4m3_encode.restype = C.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [C.c_float]
+            lib.oracle_e2m1_value.restype = C.c_float
+            lib.oracle_e2m1_value.argtypes = [C.c_uint8]
+            lib.oracle_e2m1_encode.restype = C.c_uint8
+            lib.oracle_e2m1_encode.argtypes = [C.c_float]
+            lib.oracle_tensor_scales.restype = None
+            lib.oracle_tensor_scales.argtypes = [C.c_float, C.c_int, P, P]
+            lib.oracle_nvfp4_block.restype = None
+            lib.oracle_nvfp4_block.argtypes = [P, i64, C.c_float, C.c_int, P, P, P, P]
+            lib.oracle_amax_bf16.restype = C.c_float
+            lib.oracle_amax_bf16.argtypes = [P, i64]
+            for name in ("oracle_nvfp4_quantize", "oracle_nvfp4_quantize_colwise"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [P, i64, i64, i64, u32, P, P, P, P, P]
+            for name in ("oracle_nvfp4_dequant", "oracle_nvfp4_dequant_t"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [P, P, P, i64, i64, i64, P]
+            lib.oracle_act_quantize_per_token.restype = None
+            lib.oracle_act_quantize_per_token.argtypes = [P, i64, i64, u32, P, P, P, P]
+            lib.oracle_nf4_codebook.restype = None
+            lib.oracle_nf4_codebook.argtypes = [P]
+            lib.oracle_nf4_quantize.restype = None
+            lib.oracle_nf4_quantize.argtypes = [P, i64, i64, i64, P, P, P]
+            lib.oracle_nf4_dequant.restype = None
+            lib.oracle_nf4_dequant.argtypes = [P, P, i64, i64, i64, P]
+            lib.oracle_routed_union.restype = None
+            lib.oracle_routed_union.argtypes = [P, i64, i64, i64, P, P, P]
+            lib.oracle_nf4_dequant_routed.restype = None
+            lib.oracle_nf4_dequant_routed.argtypes = [P, P, i64, i64, i64, P, i64, i64, P, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _u16(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("bf16 inputs are passed as uint16 bit patterns")
+    return x
+
+
+# --- scalar formats --------------------------------------------------------
+
+def bf16_to_f32(h: int) -> float:
+    return _load().oracle_bf16_to_f32(int(h))
+
+
+def f32_to_bf16(x: float) -> int:
+    return int(_load().oracle_f32_to_bf16(float(x)))
+
+
+def e4m3_value(c: int) -> float:
+    return _load().oracle_e4m3_value(int(c))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def e2m1_value(c: int) -> float:
+    return _load().oracle_e2m1_value(int(c))
+
+
+def e2m1_encode(x: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(x)))
+
+
+def f32_to_bf16_array(x: np.ndarray) -> np.ndarray:
+    f = _load().oracle_f32_to_bf16
+    x = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([f(float(v)) for v in x], dtype=np.uint16)
+
+
+def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
+    f = _load().oracle_e4m3_encode
+    x = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([f(float(v)) for v in x], dtype=np.uint8)
+
+
+def e2m1_encode_array(x: np.ndarray) -> np.ndarray:
+    f = _load().oracle_e2m1_encode
+    x = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([f(float(v)) for v in x], dtype=np.uint8)
+
+
+def tensor_scales(amax: float, four_over_six: bool):
+    G = C.c_float()
+    E = C.c_float()
+    _load().oracle_tensor_scales(float(amax), int(bool(four_over_six)), C.byref(G), C.byref(E))
+    return G.value, E.value
+
+
+def nvfp4_block(x16: np.ndarray, E: float, four_over_six: bool, stride: int = 1):
+    """One block: returns (scale_byte, codes[16], sse6, sse4)."""
+    x16 = _u16(x16)
+    s = C.c_uint8()
+    codes = np.zeros(16, dtype=np.uint8)
+    e6 = C.c_float()
+    e4 = C.c_float()
+    _load().oracle_nvfp4_block(_p(x16), int(stride), float(E), int(bool(four_over_six)),
+                               C.byref(s), _p(codes), C.byref(e6), C.byref(e4))
+    return int(s.value), codes, e6.value, e4.value
+
+
+def amax_bf16(x: np.ndarray) -> float:
+    x = _u16(x)
+    return _load().oracle_amax_bf16(_p(x), x.size)
+
+
+# --- tensor-level NVFP4 -----------------------------------------------------
+
+def _flags(four_over_six: bool, amax_given: bool) -> int:
+    return (FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax_given else 0)
+
+
+def nvfp4_quantize(w: np.ndarray, four_over_six: bool = False, amax: np.ndarray | None = None):
+    """Rowwise NVFP4 of w [nexp, rows, cols] (uint16 bf16 bits).
+
+    Returns dict(codes, scales, amax, G, status)."""
+    w = _u16(w)
+    nexp, rows, cols = w.shape
+    codes = np.zeros((nexp, rows, cols // 2), np.uint8)
+    scales = np.zeros((nexp, rows, cols // 16), np.uint8)
+    am = np.zeros(nexp, np.float32) if amax is None else np.array(amax, np.float32).copy()
+    G = np.zeros(nexp, np.float32)
+    st = C.c_int(0)
+    _load().oracle_nvfp4_quantize(_p(w), nexp, rows, cols, _flags(four_over_six, amax is not None),
+                                  _p(codes), _p(scales), _p(am), _p(G), C.byref(st))
+    return dict(codes=codes, scales=scales, amax=am, G=G, status=st.value)
+
+
+def nvfp4_quantize_colwise(w: np.ndarray, four_over_six: bool = False,
+                           amax: np.ndarray | None = None):
+    """Columnwise NVFP4 of w [nexp, rows, cols]; outputs are [nexp, cols, rows/2|rows/16]."""
+    w = _u16(w)
+    nexp, rows, cols = w.shape
+    codes = np.zeros((nexp, cols, rows // 2), np.uint8)
+    scales = np.zeros((nexp, cols, rows // 16), np.uint8)
+    am = np.zeros(nexp, np.float32) if amax is None else np.array(amax, np.float32).copy()
+    G = np.zeros(nexp, np.float32)
+    st = C.c_int(0)
+    _load().oracle_nvfp4_quantize_colwise(_p(w), nexp, rows, cols,
+                                          _flags(four_over_six, amax is not None),
+                                          _p(codes), _p(scales), _p(am), _p(G), C.byref(st))
+    return dict(codes=codes, scales=scales, amax=am, G=G, status=st.value)
+
+
+def nvfp4_dequant(codes: np.ndarray, scales: np.ndarray, G: np.ndarray, rows: int, cols: int):
+    nexp = G.size
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    G = np.ascontiguousarray(G, np.float32)
+    dst = np.zeros((nexp, rows, cols), np.uint16)
+    _load().oracle_nvfp4_dequant(_p(codes), _p(scales), _p(G), nexp, rows, cols, _p(dst))
+    return dst
+
+
+def nvfp4_dequant_t(codes: np.ndarray, scales: np.ndarray, G: np.ndarray, rows: int, cols: int):
+    nexp = G.size
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    G = np.ascontiguousarray(G, np.float32)
+    dst = np.zeros((nexp, cols, rows), np.uint16)
+    _load().oracle_nvfp4_dequant_t(_p(codes), _p(scales), _p(G), nexp, rows, cols, _p(dst))
+    return dst
+
+
+def act_quantize_per_token(x: np.ndarray, four_over_six: bool = True):
+    x = _u16(x)
+    T, H = x.shape
+    codes = np.zeros((T, H // 2), np.uint8)
+    scales = np.zeros((T, H // 16), np.uint8)
+    ts = np.zeros(T, np.float32)
+    st = C.c_int(0)
+    _load().oracle_act_quantize_per_token(_p(x), T, H, _flags(four_over_six, False),
+                                          _p(codes), _p(scales), _p(ts), C.byref(st))
+    return dict(codes=codes, scales=scales, token_scale=ts, status=st.value)
+
+
+# --- NF4 ----------------------------------------------------------------------
+
+def nf4_codebook() -> np.ndarray:
+    cb = np.zeros(16, np.float32)
+    _load().oracle_nf4_codebook(_p(cb))
+    return cb
+
+
+def nf4_quantize(w: np.ndarray):
+    w = _u16(w)
+    nexp, rows, cols = w.shape
+    codes = np.zeros((nexp, rows, cols // 2), np.uint8)
+    absmax = np.zeros((nexp, rows, cols // 64), np.float32)
+    st = C.c_int(0)
+    _load().oracle_nf4_quantize(_p(w), nexp, rows, cols, _p(codes), _p(absmax), C.byref(st))
+    return dict(codes=codes, absmax=absmax, status=st.value)
+
+
+def nf4_dequant(codes: np.ndarray, absmax: np.ndarray, nexp: int, rows: int, cols: int):
+    codes = np.ascontiguousarray(codes, np.uint8)
+    absmax = np.ascontiguousarray(absmax, np.float32)
+    dst = np.zeros((nexp, rows, cols), np.uint16)
+    _load().oracle_nf4_dequant(_p(codes), _p(absmax), nexp, rows, cols, _p(dst))
+    return dst
+
+
+def routed_union(topk: np.ndarray, nexp: int):
+    topk = np.ascontiguousarray(topk, np.int32)
+    T, k = topk.shape
+    hit = np.zeros(nexp, np.int32)
+    n = C.c_int32(0)
+    st = C.c_int(0)
+    _load().oracle_routed_union(_p(topk), T, k, nexp, _p(hit), C.byref(n), C.byref(st))
+    return hit, n.value, st.value
+
+
+def nf4_dequant_routed(codes: np.ndarray, absmax: np.ndarray, nexp: int, rows: int, cols: int,
+                       topk: np.ndarray, dst: np.ndarray):
+    """Dequantises the routed experts into dst (modified in place)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    absmax = np.ascontiguousarray(absmax, np.float32)
+    topk = np.ascontiguousarray(topk, np.int32)
+    assert dst.dtype == np.uint16 and dst.flags.c_contiguous and dst.shape == (nexp, rows, cols)
+    T, k = topk.shape
+    hit = np.zeros(nexp, np.int32)
+    n = C.c_int32(0)
+    st = C.c_int(0)
+    _load().oracle_nf4_dequant_routed(_p(codes), _p(absmax), nexp, rows, cols, _p(topk), T, k,
+                                      _p(dst), _p(hit), C.byref(n), C.byref(st))
+    return hit, n.value, st.value
