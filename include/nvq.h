@@ -1,0 +1,249 @@
+/*
+ * nvq.h -- C ABI of libnvq: block-scaled 4-bit quantisation of routed
+ * mixture-of-experts weights and activations on one GB300 (sm_103a).
+ *
+ * Sources the operations restate (cited by page title and section):
+ *   [P1] "Getting GLM-5.2 NVFP4 Post-Training off the ground", Part I,
+ *        "Why can't we just transpose the one copy?" and "The bottom line".
+ *   [P4] "The 4-bitter Lesson: Balancing Stability and Performance in NVFP4
+ *        RL", "Key claims" and "Method".
+ *   [P5] "nf4moe -- QLoRA for a 743B Fused-MoE", "Why every quantizer misses
+ *        95% of the model" and "The fix: dequant-on-forward for routed experts".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers.  Every tensor argument is a DEVICE pointer on the current
+ *    CUDA device, except where a comment says "host".  The caller owns and
+ *    allocates every buffer; the library allocates nothing, keeps no state
+ *    between calls and never synchronises the host.  Bulk buffers (bf16
+ *    inputs and outputs, codes, scales, absmax) must be 16-byte aligned;
+ *    FP32 and int32 arrays 4-byte aligned.
+ *  - bf16 tensors are passed as uint16_t bit patterns.  Shapes are int64.
+ *    An expert stack is row-major [nexp, rows, cols] with cols contiguous;
+ *    for an expert weight used as F.linear(x, W[e]) rows = out, cols = in
+ *    ([P5] "Why every quantizer misses 95% of the model").
+ *  - Packing.  Two 4-bit codes per byte, element 2j in the low nibble and
+ *    element 2j+1 in the high nibble.  Block scales are one byte per block,
+ *    stored linearly (row-major over blocks, no swizzle).
+ *  - Asynchrony.  A call validates its arguments on the host, enqueues its
+ *    kernels on `stream` and returns.  The return value reports only what is
+ *    known at that point: a validation error (no work is enqueued) or a
+ *    launch error (NVQ_ERR_CUDA).  A zero-sized problem returns NVQ_OK and
+ *    enqueues only what still has to be written (per-slice amax and tensor
+ *    scales of empty slices, n_hit of an empty routing).
+ *  - Device status word.  `status` (nullable, device int) receives, by
+ *    atomic OR, data-dependent conditions found while the kernels run:
+ *    NVQ_STATUS_NONFINITE when an amax / absmax is NaN or infinite (those
+ *    outputs are then unspecified) and NVQ_STATUS_BAD_INDEX when a router
+ *    index lies outside [0, nexp) (the index is ignored).  Kernels never trap.
+ *  - Calls on different streams that write the same buffers race; the
+ *    library is otherwise thread-safe (it has no global mutable state).
+ */
+#ifndef NVQ_H
+#define NVQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define NVQ_API __attribute__((visibility("default")))
+#else
+#define NVQ_API
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* nvq_stream_t;
+
+/* Return codes. */
+enum nvq_status_code {
+  NVQ_OK = 0,
+  NVQ_ERR_NULL = 1,   /* a required pointer is NULL                          */
+  NVQ_ERR_ALIGN = 2,  /* a pointer violates its alignment rule               */
+  NVQ_ERR_SHAPE = 3,  /* negative size, divisibility rule broken, overflow   */
+  NVQ_ERR_FLAGS = 4,  /* unknown flag bit                                    */
+  NVQ_ERR_DEVICE = 5, /* no CUDA device, or the current device is not sm_103 */
+  NVQ_ERR_CUDA = 6    /* a CUDA launch failed                                */
+};
+
+/* Flag bits of the quantising calls. */
+enum nvq_flags {
+  /* Four-Over-Six ([P4] "Method"): each block tries its amax mapped to 6 and
+     to 4 and keeps the scale with the lower FP32 block squared error; a tie
+     keeps 6.  Also sets the largest target block scale M to 256 instead of
+     448 (see nvfp4_quantize).                                              */
+  NVQ_4OVER6 = 1u << 0,
+  /* amax[] is an input (the caller's per-slice absolute maximum) instead of
+     being computed; lets a caller skip the reduction pass.                 */
+  NVQ_AMAX_GIVEN = 1u << 1
+};
+
+/* Bits of the device status word. */
+enum nvq_device_status {
+  NVQ_STATUS_NONFINITE = 1,
+  NVQ_STATUS_BAD_INDEX = 2
+};
+
+/* Library version, (major << 16) | minor. */
+NVQ_API int nvq_version(void);
+
+/* Static text for a return code (never NULL). */
+NVQ_API const char* nvq_status_string(int code);
+
+/*
+ * nvfp4_quantize -- rowwise NVFP4 quantisation of an expert stack.
+ * [P1] "Why can't we just transpose the one copy?": 4-bit E2M1 values, one
+ * FP8 E4M3 scale per 16-element block along one axis, one FP32 global scale;
+ * rowwise blocks are 1x16 along `in` (= cols).  [P4] "Key claims": round to
+ * nearest even, no stochastic rounding.
+ *
+ * Per expert slice e: amax_e = max|w| (or given), G_e = amax_e / (6*M) with
+ * M = 448, or 256 under NVQ_4OVER6; E_e = min(1/G_e, FLT_MAX).  Per block of
+ * 16: t_i = w_i*E_e, a = max|t_i|, S = E4M3(a/6) (or the Four-Over-Six
+ * choice between E4M3(a/6) and E4M3(a/4)), code_i = E2M1(t_i * (1/S)); E4M3
+ * and E2M1 round to nearest even and saturate (448, 6); S = 0 gives
+ * sign-only codes.
+ *
+ *   w        in   bf16 [nexp, rows, cols]; cols % 16 == 0
+ *   codes    out  u8   [nexp, rows, cols/2]
+ *   scales   out  u8   [nexp, rows, cols/16]  E4M3 bytes
+ *   amax     in/out f32 [nexp]  (input iff NVQ_AMAX_GIVEN; empty slices give 0)
+ *   tensor_scale out f32 [nexp] G_e
+ *   status   out  device int, nullable (with NVQ_AMAX_GIVEN the input is not
+ *            scanned, so only a non-finite given amax is reported)
+ */
+NVQ_API int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols,
+                   unsigned flags, uint8_t* codes, uint8_t* scales, float* amax,
+                   float* tensor_scale, int* status, nvq_stream_t stream);
+
+/*
+ * nvfp4_quantize_dual -- rowwise AND columnwise NVFP4 from one read of w.
+ * [P1] "Why can't we just transpose the one copy?": the two copies are two
+ * independent quantisations of the same weight, rowwise blocks 1x16 along
+ * `in` and columnwise blocks 16x1 along `out`, each with its own scales; the
+ * columnwise copy is K-major for dgrad, i.e. stored as the transpose.  Both
+ * use the same per-expert G_e.  Same arithmetic and flags as nvfp4_quantize.
+ *
+ *   w           in   bf16 [nexp, out, in]; out % 16 == 0, in % 16 == 0
+ *   codes_row   out  u8 [nexp, out, in/2]     scales_row out u8 [nexp, out, in/16]
+ *   codes_col   out  u8 [nexp, in, out/2]     scales_col out u8 [nexp, in, out/16]
+ *   amax, tensor_scale, status as in nvfp4_quantize
+ */
+NVQ_API int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in,
+                        unsigned flags, uint8_t* codes_row, uint8_t* scales_row,
+                        uint8_t* codes_col, uint8_t* scales_col, float* amax,
+                        float* tensor_scale, int* status, nvq_stream_t stream);
+
+/*
+ * nvfp4_dequant -- DQ(Q(w)) in the layout of the codes.
+ * [P1] "The bottom line" and [P4] "Method" (dequantised backward):
+ * y = bf16( (|c| * S) * G_e ) with the sign of the code; |c|*S is exact,
+ * the product with G_e is one FP32 rounding, the bf16 conversion rounds to
+ * nearest even.
+ *
+ *   codes in u8 [nexp, rows, cols/2]; scales in u8 [nexp, rows, cols/16];
+ *   tensor_scale in f32 [nexp]; dst out bf16 [nexp, rows, cols]; cols % 16 == 0
+ */
+NVQ_API int nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                  int64_t nexp, int64_t rows, int64_t cols, uint16_t* dst,
+                  nvq_stream_t stream);
+
+/*
+ * nvfp4_dequant_t -- DQ(Q(w)) of the ROWWISE copy written transposed, the
+ * bf16 operand of the dgrad product dX = dY*W ([P1] "The bottom line": keep
+ * only the rowwise copy, dequantise it to bf16 and run dgrad in bf16, where
+ * the transposed view is free).  Values as in nvfp4_dequant.
+ *
+ *   codes_row in u8 [nexp, out, in/2]; scales_row in u8 [nexp, out, in/16];
+ *   tensor_scale in f32 [nexp]; dst out bf16 [nexp, in, out];
+ *   out % 16 == 0, in % 16 == 0
+ */
+NVQ_API int nvfp4_dequant_t(const uint8_t* codes_row, const uint8_t* scales_row,
+                    const float* tensor_scale, int64_t nexp, int64_t out, int64_t in,
+                    uint16_t* dst, nvq_stream_t stream);
+
+/*
+ * act_quantize_per_token -- NVFP4 activations with one FP32 scale per token.
+ * [P4] "Key claims" and "Method": the scale of each token is computed over
+ * the hidden dimension inside the quantising kernel, which emits the packed
+ * codes, the per-16 E4M3 scales and the per-token FP32 scale in one pass; no
+ * state is shared across tokens.  Per row: the nvfp4_quantize arithmetic with
+ * the row as the slice.
+ *
+ *   x in bf16 [T, H], H % 16 == 0; codes out u8 [T, H/2];
+ *   scales out u8 [T, H/16]; token_scale out f32 [T]; flags: NVQ_4OVER6 only
+ */
+NVQ_API int act_quantize_per_token(const uint16_t* x, int64_t T, int64_t H, unsigned flags,
+                           uint8_t* codes, uint8_t* scales, float* token_scale,
+                           int* status, nvq_stream_t stream);
+
+/*
+ * nf4_quantize -- NF4 blockwise quantisation, blocksize 64
+ * ([P5] "The fix": each expert slice stored as NF4 with one absmax per 64
+ * elements).  Per block: absmax = max|x| (FP32), v = x * (1/absmax) (0 when
+ * absmax = 0), code = nearest of the 16 NF4 levels (see nvq_nf4_codebook),
+ * an exact midpoint going to the lower level.
+ *
+ *   w in bf16 [nexp, rows, cols], cols % 64 == 0;
+ *   codes out u8 [nexp, rows, cols/2]; absmax out f32 [nexp, rows, cols/64]
+ */
+NVQ_API int nf4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols,
+                 uint8_t* codes, float* absmax, int* status, nvq_stream_t stream);
+
+/*
+ * nf4_dequant -- full-stack NF4 dequantisation, y = bf16(level[c] * absmax).
+ *   codes in [nexp, rows, cols/2]; absmax in [nexp, rows, cols/64];
+ *   dst out bf16 [nexp, rows, cols]
+ */
+NVQ_API int nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp, int64_t rows,
+                int64_t cols, uint16_t* dst, nvq_stream_t stream);
+
+/*
+ * nf4_dequant_routed -- dequant-on-forward of only the experts the router hit
+ * ([P5] "The fix": the union of top_k_index is formed once, and only those
+ * experts are dequantised).  The union is computed on the device and consumed
+ * there: no host synchronisation at all.
+ *
+ *   codes, absmax  in   as nf4_dequant
+ *   topk_idx       in   int32 [T, k] router choices (may be NULL when T*k == 0)
+ *   dst            out  bf16 [nexp, rows, cols]; only hit slices are written
+ *   hit_list       out  int32 [nexp]: hit experts ascending, then -1
+ *   n_hit          out  int32 [1]: number of hit experts
+ *   status         out  nullable; NVQ_STATUS_BAD_INDEX for ignored indices
+ */
+NVQ_API int nf4_dequant_routed(const uint8_t* codes, const float* absmax, int64_t nexp, int64_t rows,
+                       int64_t cols, const int32_t* topk_idx, int64_t T, int64_t k,
+                       uint16_t* dst, int32_t* hit_list, int32_t* n_hit, int* status,
+                       nvq_stream_t stream);
+
+/*
+ * nvq_nf4_codebook -- copies the 16 NF4 levels the kernels use (ascending,
+ * level 7 = 0, levels 0 and 15 = -1 and +1) into `out` (HOST, 16 floats).
+ * The levels are standard-normal quantiles, 7 negative, zero, 8 positive,
+ * at probabilities evenly spaced from 1/2 to 31/32 on each side, normalised
+ * to [-1, 1] (the construction behind NF4 in [P5] "The fix").
+ */
+NVQ_API int nvq_nf4_codebook(float* out);
+
+/*
+ * nvq_debug_convert -- runs one device rounding primitive elementwise, for
+ * conversion sweeps against an independent implementation.
+ *   kind 0: f32 -> E4M3 byte (RNE, satfinite); in f32[n], out u8[n]
+ *   kind 1: f32 pair -> byte of two E2M1 codes (RNE, satfinite, sign in bit 3);
+ *           in f32[2n], out u8[n]
+ *   kind 2: f32 -> bf16 (RNE); in f32[n], out u16[n]
+ *   kind 3: f32 a -> E4M3(a/6) byte via the block-scale path; in f32[n], out u8[n]
+ *   kind 4: E4M3 byte -> f32 value; in u8[n], out f32[n]
+ *   kind 5: byte of two E2M1 codes -> two f32 (low nibble first); in u8[n], out f32[2n]
+ *   kind 6: f32 a -> E4M3(a/4) byte via the block-scale path; in f32[n], out u8[n]
+ * kind 1 reads n PAIRS of f32 (element 2i goes to the low nibble of byte i).
+ */
+NVQ_API int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVQ_H */

@@ -81,6 +81,10 @@ def _load():
                 f.argtypes = [P, P, P, i64, i64, i64, P]
             lib.oracle_act_quantize_per_token.restype = None
             lib.oracle_act_quantize_per_token.argtypes = [P, i64, i64, u32, P, P, P, P]
+            for name in ("oracle_e4m3_encode_n", "oracle_e2m1_encode_n", "oracle_f32_to_bf16_n"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [P, P, i64]
             lib.oracle_nf4_codebook.restype = None
             lib.oracle_nf4_codebook.argtypes = [P]
             lib.oracle_nf4_quantize.restype = None
@@ -134,21 +138,24 @@ def e2m1_encode(x: float) -> int:
 
 
 def f32_to_bf16_array(x: np.ndarray) -> np.ndarray:
-    f = _load().oracle_f32_to_bf16
-    x = np.asarray(x, dtype=np.float32).ravel()
-    return np.array([f(float(v)) for v in x], dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.zeros(x.size, np.uint16)
+    _load().oracle_f32_to_bf16_n(_p(x), _p(out), x.size)
+    return out
 
 
 def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
-    f = _load().oracle_e4m3_encode
-    x = np.asarray(x, dtype=np.float32).ravel()
-    return np.array([f(float(v)) for v in x], dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.zeros(x.size, np.uint8)
+    _load().oracle_e4m3_encode_n(_p(x), _p(out), x.size)
+    return out
 
 
 def e2m1_encode_array(x: np.ndarray) -> np.ndarray:
-    f = _load().oracle_e2m1_encode
-    x = np.asarray(x, dtype=np.float32).ravel()
-    return np.array([f(float(v)) for v in x], dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.zeros(x.size, np.uint8)
+    _load().oracle_e2m1_encode_n(_p(x), _p(out), x.size)
+    return out
 
 
 def tensor_scales(amax: float, four_over_six: bool):

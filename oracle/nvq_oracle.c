@@ -558,3 +558,23 @@ ORACLE_API void oracle_nf4_dequant_routed(const uint8_t* codes, const float* abs
         nf4_dequant_range(codes + e * slice / 2, absmax + e * slice / 64, slice, dst + e * slice);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Array forms of the scalar conversions (loops over the definitions above,  */
+/* for conversion sweeps).                                                   */
+/* ------------------------------------------------------------------------ */
+
+ORACLE_API void oracle_e4m3_encode_n(const float* x, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+ORACLE_API void oracle_e2m1_encode_n(const float* x, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e2m1_encode(x[i]);
+}
+
+ORACLE_API void oracle_f32_to_bf16_n(const float* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_f32_to_bf16(x[i]);
+}

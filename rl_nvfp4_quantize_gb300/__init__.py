@@ -1,0 +1,248 @@
+"""Block-scaled 4-bit quantisation of routed-MoE weights and activations on GB300.
+
+Thin Python binding over the C ABI of ``libnvq.so`` (declared in
+``include/nvq.h``).  Every function here only marshals arguments: it checks
+dtypes and shapes, allocates outputs with PyTorch when the caller passes
+none, and calls the C entry point of the same name on the current CUDA
+stream.  All arithmetic runs in the library's CUDA kernels; there is no CPU
+fallback -- importing this package fails if the library is missing or cannot
+be loaded.
+
+Sources restated by the kernels: "Getting GLM-5.2 NVFP4 Post-Training off the
+ground" (NVFP4 rowwise/columnwise copies, dequantised bf16 backward), "The
+4-bitter Lesson" (round-to-nearest, Four-Over-Six, per-token FP32 activation
+scales) and "nf4moe -- QLoRA for a 743B Fused-MoE" (NF4 blocksize 64,
+dequant-on-forward of the routed experts).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+__all__ = [
+    "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX",
+    "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t",
+    "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed",
+    "nf4_codebook", "debug_convert", "lib", "library_path",
+]
+
+FLAG_4OVER6 = 1
+FLAG_AMAX_GIVEN = 2
+STATUS_NONFINITE = 1
+STATUS_BAD_INDEX = 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libnvq.so")
+
+
+class NvqError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = lib.nvq_status_string(code).decode() if lib else str(code)
+        super().__init__("%s failed: %s (code %d)" % (fn, msg, code))
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(library_path):
+        raise ImportError("libnvq.so is not built (run __graft_entry__.build() or "
+                          "python rl_nvfp4_quantize_gb300/build.py)")
+    L = C.CDLL(library_path)
+    P, i64, u32, i32 = C.c_void_p, C.c_int64, C.c_uint, C.c_int
+    sig = {
+        "nvq_version": ([], i32),
+        "nvq_status_string": ([i32], C.c_char_p),
+        "nvfp4_quantize": ([P, i64, i64, i64, u32, P, P, P, P, P, P], i32),
+        "nvfp4_quantize_dual": ([P, i64, i64, i64, u32, P, P, P, P, P, P, P, P], i32),
+        "nvfp4_dequant": ([P, P, P, i64, i64, i64, P, P], i32),
+        "nvfp4_dequant_t": ([P, P, P, i64, i64, i64, P, P], i32),
+        "act_quantize_per_token": ([P, i64, i64, u32, P, P, P, P, P], i32),
+        "nf4_quantize": ([P, i64, i64, i64, P, P, P, P], i32),
+        "nf4_dequant": ([P, P, i64, i64, i64, P, P], i32),
+        "nf4_dequant_routed": ([P, P, i64, i64, i64, P, i64, i64, P, P, P, P, P], i32),
+        "nvq_nf4_codebook": ([P], i32),
+        "nvq_debug_convert": ([i32, P, P, i64, P], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    return L
+
+
+lib = None
+lib = _load()
+
+
+# ---------------------------------------------------------------- helpers
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise NvqError(fn, rc)
+
+
+def _bf16(t, name):
+    if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+        raise TypeError("%s must be a contiguous CUDA bfloat16 tensor" % name)
+    return t
+
+
+def _as3d(w):
+    if w.dim() == 2:
+        return w.unsqueeze(0)
+    if w.dim() != 3:
+        raise ValueError("expected [nexp, rows, cols] or [rows, cols]")
+    return w
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ---------------------------------------------------------------- NVFP4
+
+def nvfp4_quantize(w, four_over_six=False, amax=None, status=None, stream=None, out=None):
+    """Rowwise NVFP4 of w [nexp, rows, cols] (bf16).  Returns a dict with
+    codes [nexp, rows, cols/2] u8, scales [nexp, rows, cols/16] u8 (E4M3),
+    amax [nexp] f32 and tensor_scale [nexp] f32."""
+    w = _as3d(_bf16(w, "w"))
+    E, R, K = w.shape
+    o = out or {}
+    codes = o.get("codes", _empty((E, R, K // 2), torch.uint8, w))
+    scales = o.get("scales", _empty((E, R, K // 16), torch.uint8, w))
+    am = amax if amax is not None else o.get("amax", _empty((E,), torch.float32, w))
+    G = o.get("tensor_scale", _empty((E,), torch.float32, w))
+    flags = (FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
+    _check("nvfp4_quantize", lib.nvfp4_quantize(_ptr(w), E, R, K, flags, _ptr(codes), _ptr(scales),
+                                                _ptr(am), _ptr(G), _ptr(status), _stream(stream)))
+    return dict(codes=codes, scales=scales, amax=am, tensor_scale=G)
+
+
+def nvfp4_quantize_dual(w, four_over_six=True, amax=None, status=None, stream=None, out=None):
+    """Rowwise and columnwise NVFP4 of w [nexp, out, in] from one read.
+    Columnwise outputs are K-major for dgrad: [nexp, in, out/2] / [nexp, in, out/16]."""
+    w = _as3d(_bf16(w, "w"))
+    E, R, K = w.shape
+    o = out or {}
+    cr = o.get("codes_row", _empty((E, R, K // 2), torch.uint8, w))
+    sr = o.get("scales_row", _empty((E, R, K // 16), torch.uint8, w))
+    cc = o.get("codes_col", _empty((E, K, R // 2), torch.uint8, w))
+    sc = o.get("scales_col", _empty((E, K, R // 16), torch.uint8, w))
+    am = amax if amax is not None else o.get("amax", _empty((E,), torch.float32, w))
+    G = o.get("tensor_scale", _empty((E,), torch.float32, w))
+    flags = (FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
+    _check("nvfp4_quantize_dual",
+           lib.nvfp4_quantize_dual(_ptr(w), E, R, K, flags, _ptr(cr), _ptr(sr), _ptr(cc), _ptr(sc),
+                                   _ptr(am), _ptr(G), _ptr(status), _stream(stream)))
+    return dict(codes_row=cr, scales_row=sr, codes_col=cc, scales_col=sc, amax=am, tensor_scale=G)
+
+
+def nvfp4_dequant(codes, scales, tensor_scale, stream=None, out=None):
+    """DQ(Q(w)) in the layout of the codes: bf16 [nexp, rows, cols]."""
+    E, R, K2 = codes.shape
+    K = K2 * 2
+    dst = out if out is not None else _empty((E, R, K), torch.bfloat16, codes)
+    _check("nvfp4_dequant", lib.nvfp4_dequant(_ptr(codes), _ptr(scales), _ptr(tensor_scale), E, R, K,
+                                              _ptr(dst), _stream(stream)))
+    return dst
+
+
+def nvfp4_dequant_t(codes_row, scales_row, tensor_scale, stream=None, out=None):
+    """DQ(Q(w)) of the rowwise copy, transposed: bf16 [nexp, in, out]."""
+    E, R, K2 = codes_row.shape
+    K = K2 * 2
+    dst = out if out is not None else _empty((E, K, R), torch.bfloat16, codes_row)
+    _check("nvfp4_dequant_t",
+           lib.nvfp4_dequant_t(_ptr(codes_row), _ptr(scales_row), _ptr(tensor_scale), E, R, K,
+                               _ptr(dst), _stream(stream)))
+    return dst
+
+
+def act_quantize_per_token(x, four_over_six=True, status=None, stream=None, out=None):
+    """NVFP4 activations [T, H] with one FP32 scale per token."""
+    x = _bf16(x, "x")
+    if x.dim() != 2:
+        raise ValueError("expected x [T, H]")
+    T, H = x.shape
+    o = out or {}
+    codes = o.get("codes", _empty((T, H // 2), torch.uint8, x))
+    scales = o.get("scales", _empty((T, H // 16), torch.uint8, x))
+    ts = o.get("token_scale", _empty((T,), torch.float32, x))
+    flags = FLAG_4OVER6 if four_over_six else 0
+    _check("act_quantize_per_token",
+           lib.act_quantize_per_token(_ptr(x), T, H, flags, _ptr(codes), _ptr(scales), _ptr(ts),
+                                      _ptr(status), _stream(stream)))
+    return dict(codes=codes, scales=scales, token_scale=ts)
+
+
+# ---------------------------------------------------------------- NF4
+
+def nf4_quantize(w, status=None, stream=None, out=None):
+    """NF4 with blocksize 64: codes [nexp, rows, cols/2], absmax [nexp, rows, cols/64]."""
+    w = _as3d(_bf16(w, "w"))
+    E, R, K = w.shape
+    o = out or {}
+    codes = o.get("codes", _empty((E, R, K // 2), torch.uint8, w))
+    absmax = o.get("absmax", _empty((E, R, K // 64), torch.float32, w))
+    _check("nf4_quantize", lib.nf4_quantize(_ptr(w), E, R, K, _ptr(codes), _ptr(absmax),
+                                            _ptr(status), _stream(stream)))
+    return dict(codes=codes, absmax=absmax)
+
+
+def nf4_dequant(codes, absmax, stream=None, out=None):
+    E, R, K2 = codes.shape
+    K = K2 * 2
+    dst = out if out is not None else _empty((E, R, K), torch.bfloat16, codes)
+    _check("nf4_dequant", lib.nf4_dequant(_ptr(codes), _ptr(absmax), E, R, K, _ptr(dst),
+                                          _stream(stream)))
+    return dst
+
+
+def nf4_dequant_routed(codes, absmax, topk_idx, dst=None, status=None, stream=None,
+                       hit_list=None, n_hit=None):
+    """Dequantises only the experts present in topk_idx [T, k] (int32) into
+    dst [nexp, rows, cols]; returns (dst, hit_list, n_hit), both device
+    tensors -- nothing is synchronised to the host."""
+    E, R, K2 = codes.shape
+    K = K2 * 2
+    if topk_idx.dtype != torch.int32 or not topk_idx.is_contiguous():
+        raise TypeError("topk_idx must be a contiguous int32 tensor")
+    T, k = topk_idx.shape
+    if dst is None:
+        dst = _empty((E, R, K), torch.bfloat16, codes)
+    hl = hit_list if hit_list is not None else _empty((E,), torch.int32, codes)
+    nh = n_hit if n_hit is not None else _empty((1,), torch.int32, codes)
+    _check("nf4_dequant_routed",
+           lib.nf4_dequant_routed(_ptr(codes), _ptr(absmax), E, R, K, _ptr(topk_idx), T, k,
+                                  _ptr(dst), _ptr(hl), _ptr(nh), _ptr(status), _stream(stream)))
+    return dst, hl, nh
+
+
+def nf4_codebook():
+    """The 16 NF4 levels used by the kernels (host float32 tensor)."""
+    out = (C.c_float * 16)()
+    _check("nvq_nf4_codebook", lib.nvq_nf4_codebook(out))
+    return torch.tensor(list(out), dtype=torch.float32)
+
+
+_DEBUG_OUT = {0: (torch.uint8, 1), 1: (torch.uint8, 1), 2: (torch.int16, 1), 3: (torch.uint8, 1),
+              4: (torch.float32, 1), 5: (torch.float32, 2), 6: (torch.uint8, 1)}
+
+
+def debug_convert(kind: int, x, stream=None):
+    """Runs one device rounding primitive elementwise (see nvq_debug_convert)."""
+    n = x.numel() // 2 if kind == 1 else x.numel()
+    dt, mult = _DEBUG_OUT[kind]
+    out = torch.empty(n * mult, dtype=dt, device=x.device)
+    _check("nvq_debug_convert", lib.nvq_debug_convert(kind, _ptr(x), _ptr(out), n, _stream(stream)))
+    return out

@@ -1,0 +1,347 @@
+// nvq_api.cu -- the C ABI of libnvq: argument validation on the host, then
+// kernel launches on the caller's stream.  See include/nvq.h for the
+// contract of every entry point.
+#include <climits>
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "nvq.h"
+#include "nvq_common.cuh"
+#include "nvq_internal.h"
+
+namespace nvq {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+int g_dev_state[kMaxDevices];  // 0 unknown, 1 known
+std::mutex g_dev_mu;
+}  // namespace
+
+const DevInfo* device_info() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev_state[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_dev[dev].sms = sms;
+    g_dev[dev].ok = (major == 10 && minor == 3) ? 1 : 0;
+    g_dev_state[dev] = 1;
+  }
+  return &g_dev[dev];
+}
+
+// ------------------------------------------------------------ debug kernels
+__global__ void k_debug_convert(int kind, const void* in, void* out, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    switch (kind) {
+      case 0: {  // f32 -> E4M3
+        const float x = static_cast<const float*>(in)[i];
+        static_cast<uint8_t*>(out)[i] = (uint8_t)(e4m3x2(x, 0.0f) & 0xff);
+        break;
+      }
+      case 1: {  // f32 pair -> E2M1x2 byte
+        const float* f = static_cast<const float*>(in);
+        uint32_t h2;
+        static_cast<uint8_t*>(out)[i] = (uint8_t)e2m1x2_enc_dec(f[2 * i], f[2 * i + 1], h2);
+        break;
+      }
+      case 2: {  // f32 -> bf16
+        const float x = static_cast<const float*>(in)[i];
+        static_cast<uint16_t*>(out)[i] = (uint16_t)(bf16x2_rn(x, 0.0f) & 0xffff);
+        break;
+      }
+      case 3: {  // a -> E4M3(a/6) via the block-scale path
+        const float a = static_cast<const float*>(in)[i];
+        static_cast<uint8_t*>(out)[i] = (uint8_t)(block_scale_bytes(a) & 0xff);
+        break;
+      }
+      case 4: {  // E4M3 byte -> f32
+        const uint8_t b = static_cast<const uint8_t*>(in)[i];
+        static_cast<float*>(out)[i] = e4m3_decode(b & 0x7f) * ((b & 0x80) ? -1.0f : 1.0f);
+        break;
+      }
+      case 5: {  // E2M1x2 byte -> two f32
+        const uint8_t b = static_cast<const uint8_t*>(in)[i];
+        const uint32_t h2 = e2m1x2_dec(b);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        static_cast<float*>(out)[2 * i] = f.x;
+        static_cast<float*>(out)[2 * i + 1] = f.y;
+        break;
+      }
+      case 6: {  // a -> E4M3(a/4) via the block-scale path
+        const float a = static_cast<const float*>(in)[i];
+        static_cast<uint8_t*>(out)[i] = (uint8_t)((block_scale_bytes(a) >> 8) & 0xff);
+        break;
+      }
+      default:
+        break;
+    }
+  }
+}
+
+cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const DevInfo* di = device_info();
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)di->sms * 8);
+  k_debug_convert<<<grid, 256, 0, s>>>(kind, in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace nvq
+
+// ---------------------------------------------------------------- the C ABI
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// a * b * c without int64 overflow (all non-negative)
+bool mul_ok(int64_t a, int64_t b, int64_t c, int64_t* out) {
+  __int128 p = (__int128)a * b * c;
+  if (p > (__int128)(INT64_MAX / 4)) return false;
+  *out = (int64_t)p;
+  return true;
+}
+
+int device_check() {
+  const nvq::DevInfo* di = nvq::device_info();
+  if (!di || !di->ok) return NVQ_ERR_DEVICE;
+  return NVQ_OK;
+}
+
+int launch_result(cudaError_t e) {
+  if (e == cudaSuccess) return NVQ_OK;
+  cudaGetLastError();
+  return NVQ_ERR_CUDA;
+}
+
+cudaStream_t cs(nvq_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Shape checks shared by the NVFP4 quantisers: non-negative sizes, per-slice
+// dimensions that fit in int, and total sizes that fit in int64.
+int check_stack(int64_t nexp, int64_t rows, int64_t cols, int64_t* total) {
+  if (nexp < 0 || rows < 0 || cols < 0) return NVQ_ERR_SHAPE;
+  if (rows > INT_MAX || cols > INT_MAX) return NVQ_ERR_SHAPE;
+  if (!mul_ok(nexp, rows, cols, total)) return NVQ_ERR_SHAPE;
+  return NVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvq_version(void) { return (1 << 16) | 0; }
+
+const char* nvq_status_string(int code) {
+  switch (code) {
+    case NVQ_OK: return "ok";
+    case NVQ_ERR_NULL: return "a required pointer is NULL";
+    case NVQ_ERR_ALIGN: return "a pointer violates its alignment rule";
+    case NVQ_ERR_SHAPE: return "invalid shape (negative, not divisible, or too large)";
+    case NVQ_ERR_FLAGS: return "unknown flag bit";
+    case NVQ_ERR_DEVICE: return "no CUDA device of compute capability 10.3 is current";
+    case NVQ_ERR_CUDA: return "a CUDA launch failed";
+    default: return "unknown status code";
+  }
+}
+
+int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, unsigned flags,
+                   uint8_t* codes, uint8_t* scales, float* amax, float* tensor_scale, int* status,
+                   nvq_stream_t stream) {
+  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_AMAX_GIVEN)) return NVQ_ERR_FLAGS;
+  int64_t total;
+  int rc = check_stack(nexp, rows, cols, &total);
+  if (rc) return rc;
+  if (cols % 16) return NVQ_ERR_SHAPE;
+  if (nexp == 0) return NVQ_OK;
+  if (!amax || !tensor_scale) return NVQ_ERR_NULL;
+  if (!aligned(amax, 4) || !aligned(tensor_scale, 4) || (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  if (total > 0) {
+    if (!w || !codes || !scales) return NVQ_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return NVQ_ERR_ALIGN;
+  }
+  if ((rc = device_check())) return rc;
+  cudaStream_t s = cs(stream);
+  const bool f46 = flags & NVQ_4OVER6;
+  if (!(flags & NVQ_AMAX_GIVEN)) {
+    if ((rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
+    if (total > 0 && (rc = launch_result(nvq::launch_amax(w, nexp, rows * cols, amax, s))))
+      return rc;
+  }
+  if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
+  return launch_result(nvq::launch_quant_tiles(w, nexp, (int)rows, (int)cols, f46, codes, scales,
+                                               nullptr, nullptr, amax, tensor_scale, status, s));
+}
+
+int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in, unsigned flags,
+                        uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
+                        uint8_t* scales_col, float* amax, float* tensor_scale, int* status,
+                        nvq_stream_t stream) {
+  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_AMAX_GIVEN)) return NVQ_ERR_FLAGS;
+  int64_t total;
+  int rc = check_stack(nexp, out, in, &total);
+  if (rc) return rc;
+  if (out % 16 || in % 16) return NVQ_ERR_SHAPE;
+  if (nexp == 0) return NVQ_OK;
+  if (!amax || !tensor_scale) return NVQ_ERR_NULL;
+  if (!aligned(amax, 4) || !aligned(tensor_scale, 4) || (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  if (total > 0) {
+    if (!w || !codes_row || !scales_row || !codes_col || !scales_col) return NVQ_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(codes_row, 16) || !aligned(scales_row, 16) ||
+        !aligned(codes_col, 16) || !aligned(scales_col, 16))
+      return NVQ_ERR_ALIGN;
+  }
+  if ((rc = device_check())) return rc;
+  cudaStream_t s = cs(stream);
+  const bool f46 = flags & NVQ_4OVER6;
+  if (!(flags & NVQ_AMAX_GIVEN)) {
+    if ((rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
+    if (total > 0 && (rc = launch_result(nvq::launch_amax(w, nexp, out * in, amax, s)))) return rc;
+  }
+  if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
+  return launch_result(nvq::launch_quant_tiles(w, nexp, (int)out, (int)in, f46, codes_row,
+                                               scales_row, codes_col, scales_col, amax,
+                                               tensor_scale, status, s));
+}
+
+int nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                  int64_t nexp, int64_t rows, int64_t cols, uint16_t* dst, nvq_stream_t stream) {
+  int64_t total;
+  int rc = check_stack(nexp, rows, cols, &total);
+  if (rc) return rc;
+  if (cols % 16) return NVQ_ERR_SHAPE;
+  if (total == 0) return NVQ_OK;
+  if (!codes || !scales || !tensor_scale || !dst) return NVQ_ERR_NULL;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(dst, 16) || !aligned(tensor_scale, 4))
+    return NVQ_ERR_ALIGN;
+  if ((rc = device_check())) return rc;
+  return launch_result(
+      nvq::launch_dequant(codes, scales, tensor_scale, nexp, rows * cols, dst, cs(stream)));
+}
+
+int nvfp4_dequant_t(const uint8_t* codes_row, const uint8_t* scales_row, const float* tensor_scale,
+                    int64_t nexp, int64_t out, int64_t in, uint16_t* dst, nvq_stream_t stream) {
+  int64_t total;
+  int rc = check_stack(nexp, out, in, &total);
+  if (rc) return rc;
+  if (out % 16 || in % 16) return NVQ_ERR_SHAPE;
+  if (total == 0) return NVQ_OK;
+  if (!codes_row || !scales_row || !tensor_scale || !dst) return NVQ_ERR_NULL;
+  if (!aligned(codes_row, 16) || !aligned(scales_row, 16) || !aligned(dst, 16) ||
+      !aligned(tensor_scale, 4))
+    return NVQ_ERR_ALIGN;
+  if ((rc = device_check())) return rc;
+  return launch_result(nvq::launch_dequant_t(codes_row, scales_row, tensor_scale, nexp, (int)out,
+                                             (int)in, dst, cs(stream)));
+}
+
+int act_quantize_per_token(const uint16_t* x, int64_t T, int64_t H, unsigned flags,
+                           uint8_t* codes, uint8_t* scales, float* token_scale, int* status,
+                           nvq_stream_t stream) {
+  if (flags & ~(unsigned)NVQ_4OVER6) return NVQ_ERR_FLAGS;
+  int64_t total;
+  int rc = check_stack(1, T, H, &total);
+  if (rc) return rc;
+  if (H % 16) return NVQ_ERR_SHAPE;
+  if (T == 0) return NVQ_OK;
+  if (!token_scale) return NVQ_ERR_NULL;
+  if (!aligned(token_scale, 4) || (status && !aligned(status, 4))) return NVQ_ERR_ALIGN;
+  if (H > 0) {
+    if (!x || !codes || !scales) return NVQ_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return NVQ_ERR_ALIGN;
+  }
+  if ((rc = device_check())) return rc;
+  cudaStream_t s = cs(stream);
+  if (H == 0) return launch_result(nvq::launch_zero_f32(token_scale, T, s));
+  return launch_result(nvq::launch_act(x, T, (int)H, (flags & NVQ_4OVER6) != 0, codes, scales,
+                                       token_scale, status, s));
+}
+
+int nf4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, uint8_t* codes,
+                 float* absmax, int* status, nvq_stream_t stream) {
+  int64_t total;
+  int rc = check_stack(nexp, rows, cols, &total);
+  if (rc) return rc;
+  if (cols % 64) return NVQ_ERR_SHAPE;
+  if (total == 0) return NVQ_OK;
+  if (!w || !codes || !absmax) return NVQ_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(absmax, 16) ||
+      (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  if ((rc = device_check())) return rc;
+  return launch_result(nvq::launch_nf4_quant(w, total, codes, absmax, status, cs(stream)));
+}
+
+int nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp, int64_t rows,
+                int64_t cols, uint16_t* dst, nvq_stream_t stream) {
+  int64_t total;
+  int rc = check_stack(nexp, rows, cols, &total);
+  if (rc) return rc;
+  if (cols % 64) return NVQ_ERR_SHAPE;
+  if (total == 0) return NVQ_OK;
+  if (!codes || !absmax || !dst) return NVQ_ERR_NULL;
+  if (!aligned(codes, 16) || !aligned(absmax, 16) || !aligned(dst, 16)) return NVQ_ERR_ALIGN;
+  if ((rc = device_check())) return rc;
+  return launch_result(nvq::launch_nf4_dequant(codes, absmax, nexp, rows * cols, nullptr, nullptr,
+                                               dst, cs(stream)));
+}
+
+int nf4_dequant_routed(const uint8_t* codes, const float* absmax, int64_t nexp, int64_t rows,
+                       int64_t cols, const int32_t* topk_idx, int64_t T, int64_t k, uint16_t* dst,
+                       int32_t* hit_list, int32_t* n_hit, int* status, nvq_stream_t stream) {
+  int64_t total;
+  int rc = check_stack(nexp, rows, cols, &total);
+  if (rc) return rc;
+  if (cols % 64 || T < 0 || k < 0) return NVQ_ERR_SHAPE;
+  if (nexp > 65536) return NVQ_ERR_SHAPE;
+  int64_t n_idx;
+  if (!mul_ok(T, k, 1, &n_idx)) return NVQ_ERR_SHAPE;
+  if (!n_hit) return NVQ_ERR_NULL;
+  if (nexp > 0 && !hit_list) return NVQ_ERR_NULL;
+  if (n_idx > 0 && !topk_idx) return NVQ_ERR_NULL;
+  if (total > 0 && (!codes || !absmax || !dst)) return NVQ_ERR_NULL;
+  if (!aligned(n_hit, 4) || (hit_list && !aligned(hit_list, 4)) ||
+      (topk_idx && !aligned(topk_idx, 4)) || (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  if (total > 0 && (!aligned(codes, 16) || !aligned(absmax, 16) || !aligned(dst, 16)))
+    return NVQ_ERR_ALIGN;
+  if ((rc = device_check())) return rc;
+  cudaStream_t s = cs(stream);
+  if ((rc = launch_result(
+           nvq::launch_routed_union(topk_idx, n_idx, (int)nexp, hit_list, n_hit, status, s))))
+    return rc;
+  if (total == 0) return NVQ_OK;
+  return launch_result(
+      nvq::launch_nf4_dequant(codes, absmax, nexp, rows * cols, hit_list, n_hit, dst, s));
+}
+
+int nvq_nf4_codebook(float* out) {
+  if (!out) return NVQ_ERR_NULL;
+  nvq::nf4_levels_host(out);
+  return NVQ_OK;
+}
+
+int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nvq_stream_t stream) {
+  if (kind < 0 || kind > 6) return NVQ_ERR_FLAGS;
+  if (n < 0) return NVQ_ERR_SHAPE;
+  if (n == 0) return NVQ_OK;
+  if (!in || !out) return NVQ_ERR_NULL;
+  int rc = device_check();
+  if (rc) return rc;
+  return launch_result(nvq::launch_debug_convert(kind, in, out, n, cs(stream)));
+}
+
+}  // extern "C"

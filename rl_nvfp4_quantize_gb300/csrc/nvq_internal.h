@@ -1,0 +1,61 @@
+// nvq_internal.h -- host-side launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvq {
+
+struct DevInfo {
+  int sms;
+  int ok;  // 1 when the device is compute capability 10.3
+};
+
+// Current device's properties, or nullptr when there is no usable device.
+const DevInfo* device_info();
+
+// Zeroes n floats (the amax accumulators) on the stream.
+cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s);
+
+// tensor_scale[e] = amax[e] / (6 M) for every slice (empty-slice case).
+cudaError_t launch_tensor_scales(const float* amax, float* G, int64_t n, bool f46, cudaStream_t s);
+
+// amax[e] = max |w| over slice e (atomic max of FP32 bit patterns; amax
+// must be zeroed first).  Sets status bit 0 for non-finite results.
+cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, float* amax,
+                        cudaStream_t s);
+
+// Rowwise (and, with codes_col != nullptr, columnwise) NVFP4 of a stack.
+cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
+                               uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
+                               uint8_t* scales_col, const float* amax, float* tensor_scale,
+                               int* status, cudaStream_t s);
+
+cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* codes,
+                       uint8_t* scales, float* token_scale, int* status, cudaStream_t s);
+
+cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const float* G,
+                           int64_t nexp, int64_t per_slice, uint16_t* dst, cudaStream_t s);
+
+cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const float* G,
+                             int64_t nexp, int out, int in, uint16_t* dst, cudaStream_t s);
+
+cudaError_t launch_nf4_quant(const uint16_t* w, int64_t n, uint8_t* codes, float* absmax,
+                             int* status, cudaStream_t s);
+
+// Dequantises whole expert slices.  With hit_list == nullptr every slice
+// 0..nexp-1 is written; otherwise the first *n_hit entries of hit_list
+// (device) name the slices.
+cudaError_t launch_nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp,
+                               int64_t per_slice, const int32_t* hit_list, const int32_t* n_hit,
+                               uint16_t* dst, cudaStream_t s);
+
+cudaError_t launch_routed_union(const int32_t* topk, int64_t n_idx, int nexp, int32_t* hit_list,
+                                int32_t* n_hit, int* status, cudaStream_t s);
+
+cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n, cudaStream_t s);
+
+// The 16 NF4 levels used by the kernels (host copy).
+void nf4_levels_host(float out[16]);
+
+}  // namespace nvq

@@ -1,0 +1,301 @@
+// nvq_nf4.cu -- NF4 kernels for sm_103a: blockwise quantisation with block
+// size 64, dequantisation of whole expert slices, the routed-expert union
+// and the routed dequant-on-forward.
+//
+// Source: "nf4moe -- QLoRA for a 743B Fused-MoE", "The fix: dequant-on-forward
+// for routed experts" (experts stored as NF4 with one absmax per 64 elements;
+// the union of top_k_index is formed once and only those experts are
+// dequantised) and "Making it fast: the step tax" (the per-step dequant cost
+// this path exists to shrink).
+#include <cfloat>
+#include <algorithm>
+#include <cstdint>
+
+#include "nvq_common.cuh"
+#include "nvq_internal.h"
+
+namespace nvq {
+
+// The 16 NF4 levels, ascending: standard-normal quantiles at probabilities
+// evenly spaced from 1/2 to 31/32 (7 steps below zero, 8 above), divided by
+// the quantile at 31/32 so the outermost levels are -1 and +1, zero exact.
+__constant__ float c_nf4[16] = {
+    -0x1.000000p+0f, -0x1.6311acp-1f, -0x1.0b8d60p-1f, -0x1.924c0ap-2f,
+    -0x1.21b102p-2f, -0x1.7851c6p-3f, -0x1.72d976p-4f, 0x0.0p+0f,
+    0x1.4421acp-4f,  0x1.47c076p-3f,  0x1.f54804p-3f,  0x1.582f80p-2f,
+    0x1.c1002ap-2f,  0x1.1eba52p-1f,  0x1.70ca9ap-1f,  0x1.000000p+0f};
+
+static const float h_nf4[16] = {
+    -0x1.000000p+0f, -0x1.6311acp-1f, -0x1.0b8d60p-1f, -0x1.924c0ap-2f,
+    -0x1.21b102p-2f, -0x1.7851c6p-3f, -0x1.72d976p-4f, 0x0.0p+0f,
+    0x1.4421acp-4f,  0x1.47c076p-3f,  0x1.f54804p-3f,  0x1.582f80p-2f,
+    0x1.c1002ap-2f,  0x1.1eba52p-1f,  0x1.70ca9ap-1f,  0x1.000000p+0f};
+
+void nf4_levels_host(float out[16]) {
+  for (int i = 0; i < 16; i++) out[i] = h_nf4[i];
+}
+
+// --------------------------------------------------------------- quantise
+// The nearest level is found through a lookup on the top 12 bits of the
+// normalised value v (sign, exponent, 3 mantissa bits).  Each such bucket
+// spans at most one eighth of an octave, and consecutive NF4 midpoints are
+// further apart than that, so a bucket holds at most one midpoint mu: the
+// code is lo + (v > mu), lo being the number of midpoints below the bucket.
+// With mu = +inf for buckets without a midpoint this reproduces exactly
+// "the number of midpoints strictly below v".
+struct __align__(8) Nf4Ent {
+  float thr;
+  int lo;
+};
+constexpr int kNf4Buckets = 4096;
+constexpr int kNqThreads = 256;
+constexpr int kNqSmem = kNf4Buckets * 8;
+
+__device__ __forceinline__ void build_nf4_buckets(Nf4Ent* tbl) {
+  float m[15];
+#pragma unroll
+  for (int j = 0; j < 15; j++) m[j] = __fmul_rn(__fadd_rn(c_nf4[j], c_nf4[j + 1]), 0.5f);
+  for (int idx = threadIdx.x; idx < kNf4Buckets; idx += blockDim.x) {
+    const uint32_t key = (uint32_t)idx & 0x7ffu;
+    const bool neg = (idx >> 11) != 0;
+    Nf4Ent ent;
+    ent.thr = __int_as_float(0x7f800000);
+    ent.lo = 0;
+    if (key < 0x7f8u) {  // finite magnitudes only
+      const float L = __uint_as_float(key << 20), U = __uint_as_float((key + 1) << 20);
+      int lo = 0;
+      if (!neg) {  // v in [L, U)
+#pragma unroll
+        for (int j = 0; j < 15; j++) {
+          if (m[j] < L) lo++;
+          else if (m[j] < U) ent.thr = m[j];
+        }
+      } else {  // v in (-U, -L]
+#pragma unroll
+        for (int j = 0; j < 15; j++) {
+          if (m[j] <= -U) lo++;
+          else if (m[j] <= -L) ent.thr = m[j];
+        }
+      }
+      ent.lo = lo;
+    }
+    tbl[idx] = ent;
+  }
+}
+
+__device__ __forceinline__ uint32_t nf4_code(float v, const Nf4Ent* tbl) {
+  const Nf4Ent e = tbl[__float_as_uint(v) >> 20];
+  return (uint32_t)(e.lo + (v > e.thr ? 1 : 0));
+}
+
+// One thread per half block (32 elements = 64 bytes); the two halves of a
+// block sit in adjacent lanes and exchange their maxima by shuffle.
+__global__ void __launch_bounds__(kNqThreads)
+    k_nf4_quant(const uint16_t* __restrict__ w, int64_t nhalf, uint8_t* __restrict__ codes,
+                float* __restrict__ absmax, int* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  Nf4Ent* const tbl = reinterpret_cast<Nf4Ent*>(smem);
+  build_nf4_buckets(tbl);
+  __syncthreads();
+  const int64_t stride = (int64_t)gridDim.x * kNqThreads;
+  // The loop bound is taken at the warp's first lane so that whole warps
+  // stay together for the shuffle; lanes past the end only skip the stores.
+  for (int64_t h = (int64_t)blockIdx.x * kNqThreads + threadIdx.x; h - (threadIdx.x & 31) < nhalf;
+       h += stride) {
+    const bool act = h < nhalf;
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) v[u] = act ? ldg_stream(w + h * 32 + u * 8) : make_uint4(0, 0, 0, 0);
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      m = umaxmag2(m, v[u].x);
+      m = umaxmag2(m, v[u].y);
+      m = umaxmag2(m, v[u].z);
+      m = umaxmag2(m, v[u].w);
+    }
+    uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
+    mm = max(mm, __shfl_xor_sync(0xffffffffu, mm, 1));
+    const float am = __uint_as_float(mm);
+    const float r = (am == 0.0f) ? 0.0f : __frcp_rn(am);
+    const float2 r2 = make_float2(r, r);
+    if (act) {
+      uint32_t out[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t o = 0;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const float2 x = __fmul2_rn(make_float2(lo_f(wv[i]), hi_f(wv[i])), r2);
+          const uint32_t b = nf4_code(x.x, tbl) | (nf4_code(x.y, tbl) << 4);
+          o |= b << (8 * i);
+        }
+        out[u] = o;
+      }
+      *reinterpret_cast<uint4*>(codes + h * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+      if ((h & 1) == 0) {
+        absmax[h >> 1] = am;
+        if (status && !isfinite(am)) atomicOr(status, kStatusNonFinite);
+      }
+    }
+  }
+}
+
+cudaError_t launch_nf4_quant(const uint16_t* w, int64_t n, uint8_t* codes, float* absmax,
+                             int* status, cudaStream_t s) {
+  static int attr_done = 0;
+  if (!attr_done) {
+    cudaError_t err = cudaFuncSetAttribute(k_nf4_quant, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kNqSmem);
+    if (err != cudaSuccess) return err;
+    attr_done = 1;
+  }
+  const int64_t nhalf = n / 32;
+  if (nhalf == 0) return cudaSuccess;
+  const DevInfo* di = device_info();
+  const int grid = (int)std::min<int64_t>((nhalf + kNqThreads - 1) / kNqThreads, (int64_t)di->sms * 6);
+  k_nf4_quant<<<grid, kNqThreads, kNqSmem, s>>>(w, nhalf, codes, absmax, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- dequant
+// y = bf16(level[c] * absmax).  A 256-entry table maps a code byte to the
+// pair (level[low nibble], level[high nibble]); one packed multiply and one
+// bf16x2 conversion finish two elements.
+constexpr int kNdThreads = 256;
+constexpr int kNdPer = 4;                                        // units per thread per item
+constexpr int64_t kNdChunk = (int64_t)kNdThreads * kNdPer * 32;  // elements per item
+
+__global__ void __launch_bounds__(kNdThreads)
+    k_nf4_dequant(const uint8_t* __restrict__ codes, const float* __restrict__ absmax,
+                  int64_t nexp, int64_t per_slice, int64_t chunks_per_slice,
+                  const int32_t* __restrict__ hit_list, const int32_t* __restrict__ n_hit,
+                  uint16_t* __restrict__ dst) {
+  __shared__ float2 pairs[256];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    pairs[i] = make_float2(c_nf4[i & 15], c_nf4[i >> 4]);
+  __syncthreads();
+  const int64_t nslots = hit_list ? (int64_t)(*n_hit) : nexp;
+  const int64_t nitems = nslots * chunks_per_slice;
+  for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
+    const int64_t slot = it / chunks_per_slice;
+    const int64_t e = hit_list ? (int64_t)hit_list[slot] : slot;
+    if (e < 0 || e >= nexp) continue;
+    const int64_t u0 = (it - slot * chunks_per_slice) * (kNdChunk / 32);
+    const int64_t units = per_slice / 32;
+    const uint8_t* cs = codes + e * (per_slice / 2);
+    const float* as = absmax + e * (per_slice / 64);
+    uint16_t* ds = dst + e * per_slice;
+#pragma unroll
+    for (int k = 0; k < kNdPer; k++) {
+      const int64_t u = u0 + k * kNdThreads + threadIdx.x;
+      if (u < units) {
+        const uint4 c = ldg_stream(cs + u * 16);
+        const float a = as[u >> 1];
+        const float2 a2 = make_float2(a, a);
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            const float2 y = __fmul2_rn(pairs[(cw[i] >> (8 * j)) & 0xff], a2);
+            o[4 * i + j] = bf16x2_rn(y.x, y.y);
+          }
+        }
+        uint4* out = reinterpret_cast<uint4*>(ds + u * 32);
+        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        out[2] = make_uint4(o[8], o[9], o[10], o[11]);
+        out[3] = make_uint4(o[12], o[13], o[14], o[15]);
+      }
+    }
+  }
+}
+
+cudaError_t launch_nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp,
+                               int64_t per_slice, const int32_t* hit_list, const int32_t* n_hit,
+                               uint16_t* dst, cudaStream_t s) {
+  const int64_t cps = (per_slice + kNdChunk - 1) / kNdChunk;
+  if (nexp == 0 || cps == 0) return cudaSuccess;
+  const DevInfo* di = device_info();
+  const int grid = (int)std::min<int64_t>(nexp * cps, (int64_t)di->sms * 8);
+  k_nf4_dequant<<<grid, kNdThreads, 0, s>>>(codes, absmax, nexp, per_slice, cps, hit_list, n_hit,
+                                           dst);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------- routed union
+// One CTA: mark every routed expert in a shared byte map, then compact the
+// map in ascending order with a block-wide scan.  No host synchronisation:
+// the hit list and its length stay on the device for the dequant kernel.
+constexpr int kUnThreads = 1024;
+
+__global__ void __launch_bounds__(kUnThreads)
+    k_routed_union(const int32_t* __restrict__ topk, int64_t n_idx, int nexp,
+                   int32_t* __restrict__ hit_list, int32_t* __restrict__ n_hit,
+                   int* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char flags[];
+  __shared__ int wsum[kUnThreads / 32];
+  __shared__ int bad_any;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwords = (nexp + 3) / 4;
+  for (int i = tid; i < nwords; i += kUnThreads) reinterpret_cast<uint32_t*>(flags)[i] = 0;
+  if (tid == 0) bad_any = 0;
+  __syncthreads();
+  int bad = 0;
+  for (int64_t i = tid; i < n_idx; i += kUnThreads) {
+    const int32_t e = topk[i];
+    if (e >= 0 && e < nexp) flags[e] = 1;
+    else bad = 1;
+  }
+  if (bad) bad_any = 1;
+  __syncthreads();
+  if (tid == 0 && bad_any && status) atomicOr(status, kStatusBadIndex);
+  // each thread owns a contiguous run of experts
+  const int per = (nexp + kUnThreads - 1) / kUnThreads;
+  const int e0 = min(tid * per, nexp), e1 = min(e0 + per, nexp);
+  int cnt = 0;
+  for (int e = e0; e < e1; e++) cnt += flags[e];
+  int incl = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v += u;
+    }
+    wsum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  int pos = incl - cnt + (warp > 0 ? wsum[warp - 1] : 0);
+  const int total = wsum[kUnThreads / 32 - 1];
+  for (int e = e0; e < e1; e++)
+    if (flags[e]) hit_list[pos++] = e;
+  for (int i = total + tid; i < nexp; i += kUnThreads) hit_list[i] = -1;
+  if (tid == 0) *n_hit = total;
+}
+
+cudaError_t launch_routed_union(const int32_t* topk, int64_t n_idx, int nexp, int32_t* hit_list,
+                                int32_t* n_hit, int* status, cudaStream_t s) {
+  static int attr_done = 0;
+  const int smem = ((nexp + 15) / 16) * 16;
+  if (!attr_done) {
+    cudaError_t err = cudaFuncSetAttribute(k_routed_union,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
+    if (err != cudaSuccess) return err;
+    attr_done = 1;
+  }
+  k_routed_union<<<1, kUnThreads, smem, s>>>(topk, n_idx, nexp, hit_list, n_hit, status);
+  return cudaGetLastError();
+}
+
+}  // namespace nvq

@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+include/nvq.h declares, validates arguments before touching the GPU, and
+carries the same NF4 level table as the oracle.  No kernel is launched."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvq.h")
+
+
+@pytest.fixture(scope="module")
+def nvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import rl_nvfp4_quantize_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^NVQ_API\s+[\w\s\*]+?\b(\w+)\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant_t", "act_quantize_per_token",
+              "nf4_quantize", "nf4_dequant_routed"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(nvq):
+    lib = C.CDLL(nvq.library_path)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strings(nvq):
+    assert nvq.lib.nvq_version() >> 16 == 1
+    for code in range(7):
+        assert nvq.lib.nvq_status_string(code)
+    assert b"unknown" in nvq.lib.nvq_status_string(99)
+
+
+def test_nf4_table_matches_oracle(nvq, oracle_mod):
+    got = nvq.nf4_codebook().numpy()
+    ref = oracle_mod.nf4_codebook()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_nf4_bucket_design_holds_for_the_table(oracle_mod):
+    """Each 12-bit bucket (sign, exponent, 3 mantissa bits) of a normalised
+    value contains at most one midpoint of the level table -- the premise of
+    the kernel's one-comparison NF4 encoder."""
+    cb = oracle_mod.nf4_codebook()
+    m = ((cb[:-1] + cb[1:]) * np.float32(0.5)).astype(np.float32)
+    keys = (m.view(np.uint32) >> 20)
+    assert len(set(keys.tolist())) == 15
+
+
+P = None
+
+
+def _vp(v):
+    return C.c_void_p(v)
+
+
+FAKE = 0x10000  # an aligned, never dereferenced address
+
+
+def test_validation_before_any_device_work(nvq):
+    L = nvq.lib
+    ok16 = _vp(FAKE)
+    # unknown flag bits
+    assert L.nvfp4_quantize(ok16, 1, 16, 16, 0x80, ok16, ok16, ok16, ok16, P, P) == 4
+    # shape rules
+    assert L.nvfp4_quantize(ok16, 1, 16, 24, 0, ok16, ok16, ok16, ok16, P, P) == 3
+    assert L.nvfp4_quantize_dual(ok16, 1, 24, 16, 0, ok16, ok16, ok16, ok16, ok16, ok16, P, P) == 3
+    assert L.nvfp4_quantize(ok16, -1, 16, 16, 0, ok16, ok16, ok16, ok16, P, P) == 3
+    assert L.nf4_quantize(ok16, 1, 4, 32, ok16, ok16, P, P) == 3
+    assert L.nvfp4_quantize(ok16, 1 << 40, 1 << 20, 1 << 20, 0, ok16, ok16, ok16, ok16, P, P) == 3
+    assert L.act_quantize_per_token(ok16, 4, 24, 0, ok16, ok16, ok16, P, P) == 3
+    assert L.act_quantize_per_token(ok16, 4, 32, 2, ok16, ok16, ok16, P, P) == 4  # amax-given not allowed
+    assert L.nf4_dequant_routed(ok16, ok16, 70000, 4, 64, ok16, 1, 1, ok16, ok16, ok16, P, P) == 3
+    # null pointers
+    assert L.nvfp4_quantize(P, 1, 16, 16, 0, ok16, ok16, ok16, ok16, P, P) == 1
+    assert L.nvfp4_quantize_dual(ok16, 1, 16, 16, 0, ok16, ok16, P, ok16, ok16, ok16, P, P) == 1
+    assert L.nvfp4_dequant_t(ok16, ok16, ok16, 1, 16, 16, P, P) == 1
+    assert L.nf4_dequant_routed(ok16, ok16, 4, 4, 64, P, 2, 2, ok16, ok16, ok16, P, P) == 1
+    assert L.nf4_dequant_routed(ok16, ok16, 4, 4, 64, ok16, 2, 2, ok16, ok16, P, P, P) == 1
+    assert L.nvq_nf4_codebook(P) == 1
+    # alignment
+    mis = _vp(FAKE + 8)
+    assert L.nvfp4_quantize(mis, 1, 16, 16, 0, ok16, ok16, ok16, ok16, P, P) == 2
+    assert L.nvfp4_dequant(ok16, ok16, _vp(FAKE + 2), 1, 16, 16, ok16, P) == 2
+    assert L.nf4_quantize(ok16, 1, 4, 64, ok16, mis, P, P) == 2
+    # empty problems succeed without a device
+    assert L.nvfp4_quantize(P, 0, 16, 16, 0, P, P, P, P, P, P) == 0
+    assert L.nvfp4_dequant(P, P, P, 3, 0, 16, P, P) == 0
+    assert L.nf4_quantize(P, 2, 0, 64, P, P, P, P) == 0
+    assert L.nvq_debug_convert(9, ok16, ok16, 4, P) == 4
+
+
+def test_valid_call_without_gpu_reports_device(nvq):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    ok16 = _vp(FAKE)
+    assert nvq.lib.nvfp4_quantize(ok16, 1, 16, 16, 0, ok16, ok16, ok16, ok16, P, P) == 5
+    assert nvq.lib.nf4_dequant_routed(ok16, ok16, 4, 4, 64, ok16, 2, 2, ok16, ok16, ok16, P, P) == 5
