@@ -1,0 +1,500 @@
+"""Benchmark of the quantisation hot path on one GB300 (or N replicas).
+
+One step is one pass of every step of the path over the full-size synthetic
+workload, through the library's public API:
+
+  * dual-layout NVFP4 + Four-Over-Six of a 256-expert MoE layer:
+    gate_up bf16 [256, 4096, 6144] and down bf16 [256, 6144, 2048]
+    (slice amax, rowwise and columnwise codes/scales from one read);
+  * DQ(Q(w)) of both rowwise copies, written transposed as bf16 for dgrad;
+  * per-token NVFP4 + Four-Over-Six of activations [16384, 6144] and
+    [32768, 2048];
+  * NF4 (blocksize 64) of gate_up, the routed union of an 8192-token top-8
+    Zipf(1.1) router and the dequant of only the routed experts.
+
+The metric is algorithmic GB/s: every input read once and every output
+written once (bf16 2 B/elem, NVFP4 0.5 + 1/16 B/elem per layout, NF4
+0.5 + 4/64 B/elem, bf16 dequant out 2 B/elem, plus the small per-slice /
+per-token FP32 scales and router indices), divided by the device time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+With --gpus N > 1 (launched by torch.distributed.run) every rank runs the
+same step on its own GPU (replicas: the path has no exchange step); value is
+the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "moe_layer_256x(4096x6144,6144x2048)+act(16384x6144,32768x2048)+nf4_routed(8192x8,zipf1.1)"
+METRIC = "quantize/dequant GB/s and % of GB300 HBM peak (NVFP4 dual+4/6, NF4 routed)"
+
+GATE_UP = (256, 4096, 6144)
+DOWN = (256, 6144, 2048)
+
+
+def set_experts(n):
+    """Reduces the expert count (profiling of small cases only)."""
+    global GATE_UP, DOWN
+    GATE_UP = (n, GATE_UP[1], GATE_UP[2])
+    DOWN = (n, DOWN[1], DOWN[2])
+ACTS = ((16384, 6144), (32768, 2048))
+TOKENS, TOPK = 8192, 8
+
+
+def nvfp4_bytes(n):           # one NVFP4 layout out
+    return n // 2 + n // 16
+
+
+def nf4_bytes(n):
+    return n // 2 + (n // 64) * 4
+
+
+# --------------------------------------------------------------- workload
+
+class Workload:
+    def __init__(self, device, seed_base=1):
+        import torch
+        from rl_nvfp4_quantize_gb300 import synth
+        self.dev = device
+        E, R, K = GATE_UP
+        self.gu = synth.expert_weights(*GATE_UP, seed=seed_base + 1, device=device)
+        self.dn = synth.expert_weights(*DOWN, seed=seed_base + 2, device=device)
+        self.x = [synth.activations(T, H, seed=seed_base + 3 + i, device=device)
+                  for i, (T, H) in enumerate(ACTS)]
+        self.topk = synth.zipf_router(TOKENS, E, TOPK, seed=seed_base + 5, device=device)
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+
+        def e(shape, dt):
+            return torch.empty(shape, dtype=dt, device=device)
+
+        def dual_out(shape):
+            n, r, k = shape
+            return dict(codes_row=e((n, r, k // 2), u8), scales_row=e((n, r, k // 16), u8),
+                        codes_col=e((n, k, r // 2), u8), scales_col=e((n, k, r // 16), u8),
+                        amax=e((n,), f32), tensor_scale=e((n,), f32))
+        self.q_gu = dual_out(GATE_UP)
+        self.q_dn = dual_out(DOWN)
+        self.dqt_gu = e((E, K, R), bf)
+        self.dqt_dn = e((DOWN[0], DOWN[2], DOWN[1]), bf)
+        self.q_x = [dict(codes=e((T, H // 2), u8), scales=e((T, H // 16), u8), token_scale=e((T,), f32))
+                    for T, H in ACTS]
+        self.nf4 = dict(codes=e((E, R, K // 2), u8), absmax=e((E, R, K // 64), f32))
+        self.nf4_dst = e(GATE_UP, bf)
+        self.hit = e((E,), torch.int32)
+        self.nhit = e((1,), torch.int32)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def calls(self):
+        """(name, callable, algorithmic bytes, kernel launches) for one step."""
+        import rl_nvfp4_quantize_gb300 as nvq
+        n_gu = GATE_UP[0] * GATE_UP[1] * GATE_UP[2]
+        n_dn = DOWN[0] * DOWN[1] * DOWN[2]
+        L = []
+        for name, w, q, n, E in (("nvfp4_quantize_dual[gate_up]", self.gu, self.q_gu, n_gu, GATE_UP[0]),
+                                 ("nvfp4_quantize_dual[down]", self.dn, self.q_dn, n_dn, DOWN[0])):
+            L.append((name, (lambda w=w, q=q: nvq.nvfp4_quantize_dual(
+                w, four_over_six=True, status=self.status, out=q)),
+                2 * n + 2 * nvfp4_bytes(n) + 8 * E, 3))
+        for name, q, dst, n, E in (("nvfp4_dequant_t[gate_up]", self.q_gu, self.dqt_gu, n_gu, GATE_UP[0]),
+                                   ("nvfp4_dequant_t[down]", self.q_dn, self.dqt_dn, n_dn, DOWN[0])):
+            L.append((name, (lambda q=q, dst=dst: nvq.nvfp4_dequant_t(
+                q["codes_row"], q["scales_row"], q["tensor_scale"], out=dst)),
+                nvfp4_bytes(n) + 2 * n + 4 * E, 1))
+        for i, (T, H) in enumerate(ACTS):
+            L.append(("act_quantize_per_token[%dx%d]" % (T, H), (lambda i=i: nvq.act_quantize_per_token(
+                self.x[i], four_over_six=True, status=self.status, out=self.q_x[i])),
+                2 * T * H + nvfp4_bytes(T * H) + 4 * T, 1))
+        L.append(("nf4_quantize[gate_up]", lambda: nvq.nf4_quantize(self.gu, status=self.status, out=self.nf4),
+                  2 * n_gu + nf4_bytes(n_gu), 1))
+        L.append(("nf4_dequant_routed[gate_up]", lambda: nvq.nf4_dequant_routed(
+            self.nf4["codes"], self.nf4["absmax"], self.topk, dst=self.nf4_dst, status=self.status,
+            hit_list=self.hit, n_hit=self.nhit), None, 2))
+        return L
+
+    def routed_bytes(self):
+        """Algorithmic bytes of the routed dequant: only the hit experts."""
+        E, R, K = GATE_UP
+        nh = int(self.nhit.item())
+        per = R * K
+        return nh * (nf4_bytes(per) + 2 * per) + TOKENS * TOPK * 4 + 4 * (E + 1)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.rows:
+            if ts < t0 - 0.2 or ts > t1 + 0.2:
+                continue
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- the oracle
+
+def host_sample(frac, wl=None, seed_base=1):
+    """Host (CPU) inputs for a proportional sample of the step: a fraction
+    `frac` of the rows of each weight stack (taken from expert 0) and of the
+    tokens of each activation tensor.  Taken from the device workload when
+    given, else generated on the host with the same distributions."""
+    import torch
+    from rl_nvfp4_quantize_gb300 import synth
+    r_gu = max(16, int(round(frac * GATE_UP[0] * GATE_UP[1])) // 16 * 16)
+    r_dn = max(16, int(round(frac * DOWN[0] * DOWN[1])) // 16 * 16)
+    assert r_gu <= GATE_UP[1] and r_dn <= DOWN[1], "sample larger than one expert"
+    toks = [max(1, int(round(frac * T))) for T, _ in ACTS]
+    if wl is not None:
+        gu = wl.gu[0:1, :r_gu].cpu()
+        dn = wl.dn[0:1, :r_dn].cpu()
+        xs = [wl.x[i][:t].cpu() for i, t in enumerate(toks)]
+    else:
+        gu = synth.expert_weights(1, r_gu, GATE_UP[2], seed=seed_base + 1)
+        dn = synth.expert_weights(1, r_dn, DOWN[2], seed=seed_base + 2)
+        xs = [synth.activations(t, H, seed=seed_base + 3 + i) for i, (t, (_, H)) in enumerate(zip(toks, ACTS))]
+    return gu, dn, xs
+
+
+def oracle_step(gu, dn, xs):
+    """One pass of the oracle over a host sample (same calls as a GPU step:
+    both-layout NVFP4 + Four-Over-Six with the slice amax, transposed
+    dequant, per-token activations, NF4 quantise and dequant).  Returns
+    (algorithmic bytes, seconds, description)."""
+    import numpy as np
+    import torch
+    import oracle
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    total_b, secs, parts = 0, 0.0, []
+    for name, w in (("gate_up", gu), ("down", dn)):
+        r, K = w.shape[1], w.shape[2]
+        x = u16(w)
+        t0 = time.perf_counter()
+        o = oracle.nvfp4_quantize(x, four_over_six=True)
+        oracle.nvfp4_quantize_colwise(x, four_over_six=True)
+        oracle.nvfp4_dequant_t(o["codes"], o["scales"], o["G"], r, K)
+        secs += time.perf_counter() - t0
+        n = r * K
+        total_b += 2 * n + 2 * nvfp4_bytes(n) + nvfp4_bytes(n) + 2 * n
+        parts.append("%s[0,:%d,:]" % (name, r))
+    for i, x in enumerate(xs):
+        t, H = x.shape
+        t0 = time.perf_counter()
+        oracle.act_quantize_per_token(u16(x), four_over_six=True)
+        secs += time.perf_counter() - t0
+        total_b += 2 * t * H + nvfp4_bytes(t * H) + 4 * t
+        parts.append("act[:%d,:%d]" % (t, H))
+    r, K = gu.shape[1], gu.shape[2]
+    t0 = time.perf_counter()
+    q = oracle.nf4_quantize(u16(gu))
+    oracle.nf4_dequant(q["codes"], q["absmax"], 1, r, K)
+    secs += time.perf_counter() - t0
+    n = r * K
+    total_b += 2 * n + nf4_bytes(n) + nf4_bytes(n) + 2 * n
+    parts.append("nf4 gate_up[0,:%d,:]" % r)
+    return total_b, secs, ", ".join(parts)
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, timed on the host on
+    a bounded proportional sample of the same workload per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    frac = args.ref_frac
+    gu, dn, xs = host_sample(frac)
+    for _ in range(args.warmup):
+        oracle_step(gu, dn, xs)
+    tot_b, tot_s, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        b, sec, desc = oracle_step(gu, dn, xs)
+        tot_b += b
+        tot_s += sec
+    value = tot_b / tot_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_fraction": frac},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "%s per step (fraction %g of the step)" % (desc, frac)},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------- main
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def setup_dist(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-frac", type=float, default=1.0 / 512)
+    ap.add_argument("--experts", type=int, default=256,
+                    help="experts per weight stack (256 = the full layer; fewer only for profiling)")
+    ap.add_argument("--only", default=None,
+                    help="run only the calls whose name contains this text (profiling)")
+    ap.add_argument("--ref-frac", type=float, default=1.0 / 8192)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.experts != 256:
+        set_experts(args.experts)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq  # noqa: F401
+    world, rank, local = setup_dist(args)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    wl = Workload(dev)
+    calls = wl.calls()
+    if args.only:
+        calls = [c for c in calls if args.only in c[0]]
+    launches_per_step = sum(c[3] for c in calls)
+
+    for _ in range(args.warmup):
+        for _, fn, _, _ in calls:
+            fn()
+    torch.cuda.synchronize()
+    routed_b = wl.routed_bytes()
+    calls = [(n, f, (b if b is not None else routed_b), k) for n, f, b, k in calls]
+    step_bytes = sum(c[2] for c in calls)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for s in range(args.steps):
+        for j, (_, fn, _, _) in enumerate(calls):
+            ev[s][j][0].record(stream)
+            fn()
+            ev[s][j][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed_max = max_over_ranks(world, elapsed)
+    ms_step = 1e3 * elapsed_max / args.steps
+    value = world * step_bytes * args.steps / elapsed_max / 1e9
+
+    per_call = []
+    for j, (name, _, b, k) in enumerate(calls):
+        ms = statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps))
+        per_call.append((name, ms, b))
+    peak, peak_src = load_peaks()
+    dom = max(per_call, key=lambda x: x[1])
+    dom_gbs = dom[2] / (dom[1] / 1e3) / 1e9
+    breakdown = {n: {"ms": round(ms, 4), "GB/s": round(b / (ms / 1e3) / 1e9, 1),
+                     "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)} for n, ms, b in per_call}
+    st = int(wl.status.item())
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(wl, calls, max(2, min(args.steps, 5)), stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, sec, desc = oracle_step(*host_sample(args.cpu_frac, wl))
+        cpu = {"value": round(b / sec / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "%s: fraction %g of one step, %.1f s single-threaded"
+                         % (desc, args.cpu_frac, sec)}
+
+    traffic = load_traffic(dom[0])
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "gate_up": list(GATE_UP), "down": list(DOWN),
+                   "activations": [list(a) for a in ACTS], "router": [TOKENS, TOPK, "zipf1.1"],
+                   "four_over_six": True, "l2": "inputs larger than L2 (gate_up 12.9 GB)",
+                   "routed_experts": int(wl.nhit.item()), "step_bytes": step_bytes,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "traffic": traffic,
+                     "peak_source": peak_src},
+        "hbm_frac_step": round(value / world / peak, 4),
+        "breakdown": breakdown,
+        "gpu_launches": launches_per_step * args.steps,
+        "status_word": st,
+        "clocks": sampler.summary(wall0, wall1),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def load_traffic(kernel_name):
+    """DRAM bytes per call of the dominant entry point from the committed ncu
+    summary, if one was taken of the current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        return d.get(kernel_name)
+    except (OSError, ValueError):
+        return None
+
+
+def measure_e2e(wl, calls, steps, stream, world):
+    """Same step through the public API with the inputs in pinned host memory:
+    every step copies its inputs host->device, runs the path, and copies the
+    quantised results back (the bf16 dequant outputs are consumed on the
+    device by the GEMMs and stay there)."""
+    import torch
+    h_in = [(t.cpu().pin_memory(), t) for t in [wl.gu, wl.dn, wl.x[0], wl.x[1], wl.topk]]
+    outs = [wl.q_gu[k] for k in ("codes_row", "scales_row", "codes_col", "scales_col", "tensor_scale")]
+    outs += [wl.q_dn[k] for k in ("codes_row", "scales_row", "codes_col", "scales_col", "tensor_scale")]
+    for q in wl.q_x:
+        outs += [q["codes"], q["scales"], q["token_scale"]]
+    outs += [wl.nf4["codes"], wl.nf4["absmax"], wl.hit, wl.nhit]
+    h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
+    bi = sum(h.numel() * h.element_size() for h, _ in h_in)
+    bo = sum(h.numel() * h.element_size() for h, _ in h_out)
+    step_bytes = sum(c[2] for c in calls)
+
+    def one():
+        for h, d in h_in:
+            d.copy_(h, non_blocking=True)
+        for _, fn, _, _ in calls:
+            fn()
+        for h, d in h_out:
+            h.copy_(d, non_blocking=True)
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    el = max_over_ranks(world, a.elapsed_time(b) / 1e3)
+    return {"value": round(world * step_bytes * steps / el / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": round(1e3 * el / steps, 3)}
+
+
+if __name__ == "__main__":
+    main()
