@@ -37,7 +37,10 @@ def _inputs():
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile the library if any source is newer than it; return its path."""
+    """Compile the library if any source is newer than it; return its path.
+    Extra nvcc flags may also come from the NVQ_NVCC_FLAGS environment
+    variable (space separated)."""
+    extra_flags = list(extra_flags) + os.environ.get("NVQ_NVCC_FLAGS", "").split()
     if not force and os.path.exists(LIB):
         newest = max(os.path.getmtime(p) for p in _inputs())
         if os.path.getmtime(LIB) >= newest:

@@ -15,6 +15,7 @@
 
 #include <cfloat>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -22,6 +23,7 @@ namespace nvq {
 
 constexpr int kStatusNonFinite = 1;
 constexpr int kStatusBadIndex = 2;
+constexpr int kStatusTimeout = 4;
 
 // ---------------------------------------------------------------- bf16 words
 // A 32-bit word holds two bf16 values; element 2k sits in the low half.
@@ -51,15 +53,15 @@ __device__ __forceinline__ float amax_of(uint32_t m) {
 }
 
 // ----------------------------------------------------------------- E4M3 table
-// One entry per non-negative E4M3 byte: its value S, the correctly rounded
-// reciprocal 1/S (0 for S = 0, so a zero scale yields sign-only codes), and
-// -S as an f16 pair for the residual FMA.
-struct __align__(16) ScaleEnt {
-  float S;
+// One 8-byte entry per E4M3 byte: the correctly rounded reciprocal 1/S (0 for
+// S = 0, so a zero scale yields sign-only codes) and -S as an f16 pair for
+// the residual FMA.  Bytes >= 0x80 never occur (scales are non-negative);
+// 0x7F (NaN) only for a non-finite amax, whose outputs are unspecified.
+struct __align__(8) ScaleEnt {
   float rcp;
   uint32_t negS2;
-  uint32_t pad;
 };
+constexpr int kScaleTableBytes = 128 * 8;
 
 // E4M3 (OCP): bias 7, 3 mantissa bits, subnormals m * 2^-9.
 __device__ __forceinline__ float e4m3_decode(uint32_t b) {
@@ -72,14 +74,15 @@ __device__ __forceinline__ void build_scale_table(ScaleEnt* tbl) {
   for (int b = threadIdx.x; b < 128; b += blockDim.x) {
     float S = e4m3_decode((uint32_t)b);
     ScaleEnt e;
-    e.S = S;
     e.rcp = (b == 0) ? 0.0f : __frcp_rn(S);
     uint32_t h = (uint32_t)__half_as_ushort(__float2half_rn(S)) ^ 0x8000u;
     e.negS2 = h | (h << 16);
-    e.pad = 0;
     tbl[b] = e;
   }
 }
+
+// f16 pair (S, S) of an entry.
+__device__ __forceinline__ uint32_t pos_s2(const ScaleEnt& e) { return e.negS2 ^ 0x80008000u; }
 
 // ------------------------------------------------------------- block scales
 // fl(a / 6): q0 = a * fl(1/6) followed by one FMA residual correction
@@ -132,6 +135,42 @@ __device__ __forceinline__ uint32_t e2m1x2_enc_dec(float lo, float hi, uint32_t&
   return byte;
 }
 
+// Eight FP32 values q[0..7] -> one word of eight E2M1 codes (q[j] in nibble
+// j).  The conversions write their bytes straight into the word.
+__device__ __forceinline__ uint32_t e2m1x8_enc(float q0, float q1, float q2, float q3, float q4,
+                                               float q5, float q6, float q7) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(q0), "f"(q1), "f"(q2), "f"(q3), "f"(q4), "f"(q5), "f"(q6), "f"(q7));
+  return w;
+}
+
+// Word of eight E2M1 codes -> the four exact f16 pairs (h[k] = codes 2k, 2k+1).
+__device__ __forceinline__ void e2m1x8_dec(uint32_t w, uint32_t h[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t e2m1x8_enc_dec(float q0, float q1, float q2, float q3,
+                                                   float q4, float q5, float q6, float q7,
+                                                   uint32_t h[4]) {
+  const uint32_t w = e2m1x8_enc(q0, q1, q2, q3, q4, q5, q6, q7);
+  e2m1x8_dec(w, h);
+  return w;
+}
+
 // Byte of two E2M1 codes -> exact f16 pair (low half = low nibble).
 __device__ __forceinline__ uint32_t e2m1x2_dec(uint32_t byte) {
   uint32_t h2;
@@ -165,6 +204,25 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   return d;
 }
 
+// bf16 pair -> FP32 pair, exactly: a mixed-precision FMA x*1 + (-0) per half
+// runs on the FMA pipe and leaves the (half-rate) ALU pipe to the
+// conversions; NVQ_WIDEN_LOGIC selects the two logic operations instead.
+__device__ __forceinline__ float2 widen2(uint32_t w) {
+#ifndef NVQ_WIDEN_LOGIC
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h, one;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "mov.b16 one, 0x3F80;\n\t"
+      "fma.rn.f32.bf16 %0, l, one, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %1, h, one, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+  return make_float2(lo, hi);
+#else
+  return make_float2(lo_f(w), hi_f(w));
+#endif
+}
+
 // ------------------------------------------------------------ global scales
 // G = amax / (6 M) and E = min(1/G, FLT_MAX), with 6M = 2688 (M = 448) or
 // 1536 (M = 256 under Four-Over-Six).
@@ -173,74 +231,55 @@ __device__ __forceinline__ void global_scales(float amax, float six_m, float& G,
   E = fminf(__frcp_rn(G), FLT_MAX);
 }
 
+// Larger magnitude of the two halves of a max-abs word, as FP32 (both halves
+// of the swapped max hold it; the high half is already an FP32 pattern).
+__device__ __forceinline__ float amax_fold(uint32_t m) {
+  const uint32_t both = maxabs2(m, __byte_perm(m, 0, 0x1032));
+  return __uint_as_float(both & 0x7fff0000u);
+}
+
 // ---------------------------------------------------------- one NVFP4 block
 // Candidate of one rowwise block: t2[k] = (t_2k, t_2k+1).  Writes the 8 code
 // bytes into two words and returns the FP32 squared error, accumulated as
 // two fused multiply-add chains (even and odd positions) added at the end.
-__device__ __forceinline__ float row_candidate(const float2 t2[8], const ScaleEnt& se,
+__device__ __forceinline__ float row_candidate(const float2 t2[8], const ScaleEnt se,
                                                uint32_t& c0, uint32_t& c1) {
   const float2 r2 = make_float2(se.rcp, se.rcp);
+  float2 q[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) q[k] = __fmul2_rn(t2[k], r2);
+  uint32_t h[8];
+  c0 = e2m1x8_enc_dec(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x, q[3].y, h);
+  c1 = e2m1x8_enc_dec(q[4].x, q[4].y, q[5].x, q[5].y, q[6].x, q[6].y, q[7].x, q[7].y, h + 4);
   float2 acc = make_float2(0.0f, 0.0f);
-  c0 = 0;
-  c1 = 0;
 #pragma unroll
   for (int k = 0; k < 8; k++) {
-    float2 q = __fmul2_rn(t2[k], r2);
-    uint32_t h2;
-    uint32_t b = e2m1x2_enc_dec(q.x, q.y, h2);
-    float2 d = resid2(h2, se.negS2, t2[k].x, t2[k].y);
+    const float2 d = resid2(h[k], se.negS2, t2[k].x, t2[k].y);
     acc = __ffma2_rn(d, d, acc);
-    if (k < 4) c0 |= b << (8 * k); else c1 |= b << (8 * (k - 4));
   }
   return __fadd_rn(acc.x, acc.y);
 }
 
-// Quantises one rowwise block given its 8 bf16x2 words and the slice's
-// encode factor E.  Outputs the two code words and the scale byte.
-template <bool F46>
-__device__ __forceinline__ void quant_row_block(const uint32_t w[8], float E, const ScaleEnt* tbl,
-                                                uint32_t& c0, uint32_t& c1, uint32_t& sb) {
-  uint32_t m = maxabs2(maxabs2(maxabs2(w[0], w[1]), maxabs2(w[2], w[3])),
-                       maxabs2(maxabs2(w[4], w[5]), maxabs2(w[6], w[7])));
-  float a = __fmul_rn(amax_of(m), E);
-  uint32_t sbytes = block_scale_bytes(a);
-  float2 t2[8];
-  const float2 E2 = make_float2(E, E);
-#pragma unroll
-  for (int k = 0; k < 8; k++) t2[k] = __fmul2_rn(make_float2(lo_f(w[k]), hi_f(w[k])), E2);
-  const uint32_t s6 = sbytes & 0x7fu;
-  float e6 = row_candidate(t2, tbl[s6], c0, c1);
-  sb = s6;
-  if (F46) {
-    const uint32_t s4 = (sbytes >> 8) & 0x7fu;
-    uint32_t d0, d1;
-    float e4 = row_candidate(t2, tbl[s4], d0, d1);
-    if (e4 < e6) {
-      c0 = d0;
-      c1 = d1;
-      sb = s4;
-    }
-  }
-}
-
-// Same as quant_row_block but with the block amax already known (as FP32).
+// Quantises one rowwise block given its 8 bf16x2 words, the block amax (FP32)
+// and the slice's encode factor E.  Outputs the two code words and the scale
+// byte.
 template <bool F46>
 __device__ __forceinline__ void quant_row_block_amax(const uint32_t w[8], float bamax, float E,
                                                      const ScaleEnt* tbl, uint32_t& c0,
                                                      uint32_t& c1, uint32_t& sb) {
-  float a = __fmul_rn(bamax, E);
-  uint32_t sbytes = block_scale_bytes(a);
+  const float a = __fmul_rn(bamax, E);
+  const uint32_t sbytes = block_scale_bytes(a);
   float2 t2[8];
   const float2 E2 = make_float2(E, E);
 #pragma unroll
-  for (int k = 0; k < 8; k++) t2[k] = __fmul2_rn(make_float2(lo_f(w[k]), hi_f(w[k])), E2);
+  for (int k = 0; k < 8; k++) t2[k] = __fmul2_rn(widen2(w[k]), E2);
   const uint32_t s6 = sbytes & 0x7fu;
-  float e6 = row_candidate(t2, tbl[s6], c0, c1);
+  const float e6 = row_candidate(t2, tbl[s6], c0, c1);
   sb = s6;
   if (F46) {
     const uint32_t s4 = (sbytes >> 8) & 0x7fu;
     uint32_t d0, d1;
-    float e4 = row_candidate(t2, tbl[s4], d0, d1);
+    const float e4 = row_candidate(t2, tbl[s4], d0, d1);
     if (e4 < e6) {
       c0 = d0;
       c1 = d1;
@@ -249,35 +288,41 @@ __device__ __forceinline__ void quant_row_block_amax(const uint32_t w[8], float 
   }
 }
 
+template <bool F46>
+__device__ __forceinline__ void quant_row_block(const uint32_t w[8], float E, const ScaleEnt* tbl,
+                                                uint32_t& c0, uint32_t& c1, uint32_t& sb) {
+  const uint32_t m = maxabs2(maxabs2(maxabs2(w[0], w[1]), maxabs2(w[2], w[3])),
+                             maxabs2(maxabs2(w[4], w[5]), maxabs2(w[6], w[7])));
+  quant_row_block_amax<F46>(w, amax_fold(m), E, tbl, c0, c1, sb);
+}
+
 // Candidate of two columnwise blocks side by side (columns j and j+1):
 // u[i] = (t_ij, t_i,j+1) for the 16 rows i of the block.  Codes of column j
-// go to cj0/cj1 and of column j+1 to ck0/ck1, each packed along the block
-// (element 2k in the low nibble of byte k).  Returns both errors.
-__device__ __forceinline__ float2 col_candidate(const float2 u[16], const ScaleEnt& sj,
-                                                const ScaleEnt& sk, uint32_t& cj0, uint32_t& cj1,
-                                                uint32_t& ck0, uint32_t& ck1) {
+// go to cj and of column j+1 to ck, each packed along the block (element 2k
+// in the low nibble of byte k).  Returns both errors, each accumulated as
+// an even-position and an odd-position chain added at the end.
+__device__ __forceinline__ float2 col_candidate(const float2 u[16], const ScaleEnt sj,
+                                                const ScaleEnt sk, uint32_t cj[2],
+                                                uint32_t ck[2]) {
   const float2 r2 = make_float2(sj.rcp, sk.rcp);
+  float2 q[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) q[i] = __fmul2_rn(u[i], r2);
+  uint32_t hj[8], hk[8];
+  cj[0] = e2m1x8_enc_dec(q[0].x, q[1].x, q[2].x, q[3].x, q[4].x, q[5].x, q[6].x, q[7].x, hj);
+  cj[1] = e2m1x8_enc_dec(q[8].x, q[9].x, q[10].x, q[11].x, q[12].x, q[13].x, q[14].x, q[15].x,
+                         hj + 4);
+  ck[0] = e2m1x8_enc_dec(q[0].y, q[1].y, q[2].y, q[3].y, q[4].y, q[5].y, q[6].y, q[7].y, hk);
+  ck[1] = e2m1x8_enc_dec(q[8].y, q[9].y, q[10].y, q[11].y, q[12].y, q[13].y, q[14].y, q[15].y,
+                         hk + 4);
   float2 accE = make_float2(0.0f, 0.0f), accO = make_float2(0.0f, 0.0f);
-  cj0 = cj1 = ck0 = ck1 = 0;
 #pragma unroll
   for (int k = 0; k < 8; k++) {
-    float2 q0 = __fmul2_rn(u[2 * k], r2);
-    float2 q1 = __fmul2_rn(u[2 * k + 1], r2);
-    uint32_t hj, hk;
-    uint32_t bj = e2m1x2_enc_dec(q0.x, q1.x, hj);
-    uint32_t bk = e2m1x2_enc_dec(q0.y, q1.y, hk);
-    float2 dj = resid2(hj, sj.negS2, u[2 * k].x, u[2 * k + 1].x);
-    float2 dk = resid2(hk, sk.negS2, u[2 * k].y, u[2 * k + 1].y);
-    float2 de = make_float2(dj.x, dk.x), dod = make_float2(dj.y, dk.y);
+    const float2 dj = resid2(hj[k], sj.negS2, u[2 * k].x, u[2 * k + 1].x);
+    const float2 dk = resid2(hk[k], sk.negS2, u[2 * k].y, u[2 * k + 1].y);
+    const float2 de = make_float2(dj.x, dk.x), dod = make_float2(dj.y, dk.y);
     accE = __ffma2_rn(de, de, accE);
     accO = __ffma2_rn(dod, dod, accO);
-    if (k < 4) {
-      cj0 |= bj << (8 * k);
-      ck0 |= bk << (8 * k);
-    } else {
-      cj1 |= bj << (8 * (k - 4));
-      ck1 |= bk << (8 * (k - 4));
-    }
   }
   return __fadd2_rn(accE, accO);
 }
@@ -288,41 +333,50 @@ template <bool F46>
 __device__ __forceinline__ void quant_col_pair(const uint32_t wc[16], float E, const ScaleEnt* tbl,
                                                uint32_t cj[2], uint32_t ck[2], uint32_t& sbj,
                                                uint32_t& sbk) {
-  uint32_t m = wc[0];
+  uint32_t m = maxabs2(wc[0], wc[1]);
 #pragma unroll
-  for (int i = 1; i < 16; i++) m = maxabs2(m, wc[i]);
+  for (int i = 2; i < 16; i++) m = maxabs2(m, wc[i]);
   m &= 0x7fff7fffu;
   const float2 E2 = make_float2(E, E);
-  float2 a = __fmul2_rn(make_float2(lo_f(m), hi_f(m)), E2);
-  float2 a6 = div6x2(a);
-  float2 a4 = __fmul2_rn(a, make_float2(0.25f, 0.25f));
-  uint32_t s6 = e4m3x2(a6.x, a6.y);  // byte 0: column j, byte 1: column j+1
-  uint32_t s4 = e4m3x2(a4.x, a4.y);
+  const float2 a = __fmul2_rn(make_float2(lo_f(m), hi_f(m)), E2);
+  const float2 a6 = div6x2(a);
+  const float2 a4 = __fmul2_rn(a, make_float2(0.25f, 0.25f));
+  const uint32_t s6 = e4m3x2(a6.x, a6.y);  // byte 0: column j, byte 1: column j+1
+  const uint32_t s4 = e4m3x2(a4.x, a4.y);
   float2 u[16];
 #pragma unroll
-  for (int i = 0; i < 16; i++) u[i] = __fmul2_rn(make_float2(lo_f(wc[i]), hi_f(wc[i])), E2);
+  for (int i = 0; i < 16; i++) u[i] = __fmul2_rn(widen2(wc[i]), E2);
   const uint32_t s6j = s6 & 0x7fu, s6k = (s6 >> 8) & 0x7fu;
-  float2 e6 = col_candidate(u, tbl[s6j], tbl[s6k], cj[0], cj[1], ck[0], ck[1]);
+  const float2 e6 = col_candidate(u, tbl[s6j], tbl[s6k], cj, ck);
   sbj = s6j;
   sbk = s6k;
   if (F46) {
     const uint32_t s4j = s4 & 0x7fu, s4k = (s4 >> 8) & 0x7fu;
-    uint32_t dj0, dj1, dk0, dk1;
-    float2 e4 = col_candidate(u, tbl[s4j], tbl[s4k], dj0, dj1, dk0, dk1);
+    uint32_t dj[2], dk[2];
+    const float2 e4 = col_candidate(u, tbl[s4j], tbl[s4k], dj, dk);
     if (e4.x < e6.x) {
-      cj[0] = dj0;
-      cj[1] = dj1;
+      cj[0] = dj[0];
+      cj[1] = dj[1];
       sbj = s4j;
     }
     if (e4.y < e6.y) {
-      ck[0] = dk0;
-      ck[1] = dk1;
+      ck[0] = dk[0];
+      ck[1] = dk[1];
       sbk = s4k;
     }
   }
 }
 
 // ------------------------------------------------------------ small helpers
+// Unsigned division by a divisor fixed at launch, for dividends below 2^31:
+// n / d = (umulhi(n, m) + n) >> s with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1 (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994).  Built on the host by
+// make_fastdiv(); the sum cannot overflow because umulhi(n, m) <= n < 2^31.
+struct FastDiv {
+  uint32_t d, m, s;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> s; }
+};
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
   uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
   int n = valid ? 16 : 0;
@@ -332,6 +386,79 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------- TMA and mbarriers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Waits for the phase of `bar` with the given parity to complete, giving up
+// after `max_tries` polls (each poll may itself block for a short,
+// hardware-defined time).  Returns false on giving up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_tries) {
+  for (uint32_t i = 0; i < max_tries; i++) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// 2-D tiled TMA load of one box at element coordinates (x, y) into shared
+// memory, completing on `bar` (x * element size must be a multiple of 16).
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tiled TMA store of one box from shared memory (x, y as above, both
+// non-negative); completion is tracked with bulk async groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y,
+                                             const void* smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   map),
+               "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders generic-proxy shared-memory writes before later TMA reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {

@@ -2,9 +2,27 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvq {
+
+struct FastDiv;
+
+// Host construction of a FastDiv for 1 <= d < 2^31.
+inline void make_fastdiv(uint32_t d, uint32_t* m, uint32_t* s) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) l++;
+  *s = l;
+  *m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+}
+
+// Encodes a 2-D tiled tensor map (row-major [dim1][dim0] of `elem_bytes`
+// elements, row pitch `stride_bytes`) with the given box and swizzle.
+// Returns false when the driver entry point is unavailable or rejects it.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t dim0, uint64_t dim1, uint64_t stride_bytes, uint32_t box0,
+                    uint32_t box1, CUtensorMapSwizzle swizzle);
 
 struct DevInfo {
   int sms;

@@ -169,20 +169,20 @@ constexpr int64_t kNdChunk = (int64_t)kNdThreads * kNdPer * 32;  // elements per
 
 __global__ void __launch_bounds__(kNdThreads)
     k_nf4_dequant(const uint8_t* __restrict__ codes, const float* __restrict__ absmax,
-                  int64_t nexp, int64_t per_slice, int64_t chunks_per_slice,
+                  int64_t nexp, int64_t per_slice, FastDiv cps,
                   const int32_t* __restrict__ hit_list, const int32_t* __restrict__ n_hit,
                   uint16_t* __restrict__ dst) {
   __shared__ float2 pairs[256];
   for (int i = threadIdx.x; i < 256; i += blockDim.x)
     pairs[i] = make_float2(c_nf4[i & 15], c_nf4[i >> 4]);
   __syncthreads();
-  const int64_t nslots = hit_list ? (int64_t)(*n_hit) : nexp;
-  const int64_t nitems = nslots * chunks_per_slice;
-  for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
-    const int64_t slot = it / chunks_per_slice;
-    const int64_t e = hit_list ? (int64_t)hit_list[slot] : slot;
+  const uint32_t nslots = hit_list ? (uint32_t)max(0, min(*n_hit, (int32_t)nexp)) : (uint32_t)nexp;
+  const uint32_t nitems = nslots * cps.d;
+  for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
+    const uint32_t slot = cps.div(it);
+    const int64_t e = hit_list ? (int64_t)hit_list[slot] : (int64_t)slot;
     if (e < 0 || e >= nexp) continue;
-    const int64_t u0 = (it - slot * chunks_per_slice) * (kNdChunk / 32);
+    const int64_t u0 = (int64_t)(it - slot * cps.d) * (kNdChunk / 32);
     const int64_t units = per_slice / 32;
     const uint8_t* cs = codes + e * (per_slice / 2);
     const float* as = absmax + e * (per_slice / 64);
@@ -219,9 +219,13 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const float* absmax, int64_
                                uint16_t* dst, cudaStream_t s) {
   const int64_t cps = (per_slice + kNdChunk - 1) / kNdChunk;
   if (nexp == 0 || cps == 0) return cudaSuccess;
+  if (nexp * cps >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
+  FastDiv fd;
+  fd.d = (uint32_t)cps;
+  make_fastdiv(fd.d, &fd.m, &fd.s);
   const DevInfo* di = device_info();
   const int grid = (int)std::min<int64_t>(nexp * cps, (int64_t)di->sms * 8);
-  k_nf4_dequant<<<grid, kNdThreads, 0, s>>>(codes, absmax, nexp, per_slice, cps, hit_list, n_hit,
+  k_nf4_dequant<<<grid, kNdThreads, 0, s>>>(codes, absmax, nexp, per_slice, fd, hit_list, n_hit,
                                            dst);
   return cudaGetLastError();
 }

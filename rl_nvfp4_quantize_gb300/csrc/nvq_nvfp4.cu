@@ -31,14 +31,14 @@ __global__ void k_zero_f32(float* p, int64_t n) {
 // with an atomic max on the FP32 bit pattern (ordered like the values for
 // non-negative floats, NaN above infinity).
 __global__ void __launch_bounds__(kAmaxThreads)
-    k_amax(const uint16_t* __restrict__ w, int64_t per_slice, int64_t chunks_per_slice,
-           int64_t nitems, float* __restrict__ amax) {
+    k_amax(const uint16_t* __restrict__ w, int64_t per_slice, FastDiv cps, uint32_t nitems,
+           float* __restrict__ amax) {
   __shared__ uint32_t red[kAmaxThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
-    const int64_t e = it / chunks_per_slice;
-    const int64_t start = (it - e * chunks_per_slice) * kAmaxChunk;
-    const uint16_t* base = w + e * per_slice;
+  for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
+    const uint32_t e = cps.div(it);
+    const int64_t start = (int64_t)(it - e * cps.d) * kAmaxChunk;
+    const uint16_t* base = w + (int64_t)e * per_slice;
     uint4 v[kAmaxVec];
 #pragma unroll
     for (int u = 0; u < kAmaxVec; u++) {
@@ -97,155 +97,218 @@ cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, floa
   const int64_t cps = (per_slice + kAmaxChunk - 1) / kAmaxChunk;
   const int64_t nitems = nexp * cps;
   if (nitems == 0) return cudaSuccess;
+  if (nitems >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
+  FastDiv fd;
+  fd.d = (uint32_t)cps;
+  make_fastdiv(fd.d, &fd.m, &fd.s);
   int grid = (int)std::min<int64_t>(nitems, (int64_t)di->sms * 8);
-  k_amax<<<grid, kAmaxThreads, 0, s>>>(w, per_slice, cps, nitems, amax);
+  k_amax<<<grid, kAmaxThreads, 0, s>>>(w, per_slice, fd, (uint32_t)nitems, amax);
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------- rowwise / dual tiles
 // A CTA of 256 threads walks tiles of 64 rows x 256 columns of one expert
-// slice (persistent grid-stride loop).  Each tile is staged in shared memory
-// with 16-byte cp.async copies, double-buffered so the next tile streams in
-// while the current one is quantised.  From the staged tile:
+// slice (persistent grid-stride loop).  One thread loads each tile with four
+// TMA box copies (64 x 64 bf16, 128-byte swizzle) into one of two shared
+// stages; the copy of the next tile runs while the current one is quantised.
+// From the staged tile:
 //   rowwise pass   : 1024 blocks of 1x16, four per thread, results stored
 //                    straight to global (8 code bytes + 1 scale byte);
-//   columnwise pass: 256 units of 16 rows x 4 columns, one per thread, two
-//                    column pairs processed with packed f32x2 arithmetic; the
+//   columnwise pass: 256 units of 16 rows x 4 columns, one per thread, each
+//                    column pair processed with packed f32x2 arithmetic; the
 //                    results are staged and written as contiguous runs of the
 //                    transposed [in, out/2] layout.
-// Staged 16-byte chunks are XOR-swizzled (chunk c lands at c ^ ((c>>3)&1))
-// so that both passes read shared memory without bank conflicts.
+// Inside a swizzled box, 16-byte chunk c of row r sits at chunk c ^ (r & 7).
+#ifndef NVQ_QT_MINB
+#define NVQ_QT_MINB 2
+#endif
 constexpr int kTR = 64, kTC = 256, kQT = 256;
-constexpr int kInStage = kTR * kTC * 2;   // 32 KiB
-constexpr int kColCodes = 4 * kTC * 8;    // [rb][col] 8 bytes
-constexpr int kColScales = 4 * kTC;       // [rb][col] 1 byte
-constexpr int kTbl = 128 * 16;
-constexpr int kQuantSmem = 2 * kInStage + kColCodes + kColScales + kTbl;
+constexpr int kBoxC = 64;                       // box columns (128 bytes)
+constexpr int kBoxBytes = kTR * kBoxC * 2;      // 8 KiB
+constexpr int kInStage = kTR * kTC * 2;         // 32 KiB (four boxes)
+constexpr int kColCodes = 4 * kTC * 8;          // [rb][col] 8 bytes
+constexpr int kColScales = 4 * kTC;             // [rb][col] 1 byte
+constexpr int kQuantSmem = 2 * kInStage + kColCodes + kColScales + kScaleTableBytes + 64;
+constexpr uint32_t kWaitTries = 1u << 22;
 
-__device__ __forceinline__ int swz(int chunk) { return chunk ^ ((chunk >> 3) & 1); }
+struct __align__(64) QuantTileArgs {
+  CUtensorMap tmap;       // w as [nexp * rows, cols] bf16, 64 x 64 boxes
+  uint8_t* codes_row;
+  uint8_t* scales_row;
+  uint8_t* codes_col;
+  uint8_t* scales_col;
+  const float* amax;
+  float* tensor_scale;
+  int* status;
+  int rows, cols;         // per slice
+  int tiles_c;            // column tiles per slice
+  uint32_t ntiles;        // all slices
+  FastDiv per_exp;        // tiles per slice
+  FastDiv by_tiles_c;
+};
 
 template <bool F46, bool DUAL>
-__global__ void __launch_bounds__(kQT, 2)
-    k_quant_tiles(const uint16_t* __restrict__ w, int rows, int cols, int tiles_r, int tiles_c,
-                  int64_t ntiles, uint8_t* __restrict__ codes_row, uint8_t* __restrict__ scales_row,
-                  uint8_t* __restrict__ codes_col, uint8_t* __restrict__ scales_col,
-                  const float* __restrict__ amax, float* __restrict__ tensor_scale,
-                  int* __restrict__ status) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint16_t* const in0 = reinterpret_cast<uint16_t*>(smem);
+__global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_constant__ QuantTileArgs A) {
+  // The kernel has no static shared memory, so the dynamic block starts at
+  // the (1 KiB aligned) base of the CTA's window, as the swizzled TMA boxes
+  // require; a misaligned base is reported instead of used.
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* const in0 = smem;
   unsigned char* const colc = smem + 2 * kInStage;
   unsigned char* const cols_s = colc + kColCodes;
   ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(cols_s + kColScales);
+  uint64_t* const bar = reinterpret_cast<uint64_t*>(cols_s + kColScales + kScaleTableBytes);
+  float* const s_E = reinterpret_cast<float*>(bar + 2);
   const int tid = threadIdx.x;
+  if (smem_u32(smem) & 1023u) {
+    if (tid == 0 && A.status) atomicOr(A.status, kStatusTimeout);
+    return;
+  }
   const float six_m = F46 ? 1536.0f : 2688.0f;
-  const int64_t per_exp = (int64_t)tiles_r * tiles_c;
+  const int rows = A.rows, cols = A.cols;
+  const int64_t cols_h = cols >> 1, cols_16 = cols >> 4, rows_h = rows >> 1, rows_16 = rows >> 4;
 
   build_scale_table(tbl);
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
 
-  auto issue = [&](int64_t t, int st) {
-    if (t < ntiles) {
-      const int64_t e = t / per_exp;
-      const int rem = (int)(t - e * per_exp);
-      const int tr = rem / tiles_c, tc = rem - tr * tiles_c;
-      const int r0 = tr * kTR, c0 = tc * kTC;
-      const int rv = min(kTR, rows - r0), cv = min(kTC, cols - c0);
-      const uint16_t* base = w + ((int64_t)e * rows + r0) * cols + c0;
-      uint16_t* dst = in0 + st * (kInStage / 2);
-#pragma unroll
-      for (int i = 0; i < (kTR * kTC / 8) / kQT; i++) {
-        const int ch = tid + i * kQT;
-        const int r = ch >> 5, cc = ch & 31;
-        const bool valid = (r < rv) && (cc * 8 < cv);
-        const uint16_t* src = valid ? base + (int64_t)r * cols + cc * 8 : w;
-        cp_async16(dst + r * kTC + swz(cc) * 8, src, valid);
-      }
-    }
-    cp_async_commit();
+  struct Tile { uint32_t e; int r0, c0, rv, cv; bool first; };
+  auto tile_of = [&](uint32_t t) {
+    Tile T;
+    T.e = A.per_exp.div(t);
+    const uint32_t rem = t - T.e * A.per_exp.d;
+    const uint32_t tr = A.by_tiles_c.div(rem);
+    const uint32_t tc = rem - tr * (uint32_t)A.tiles_c;
+    T.r0 = (int)tr * kTR;
+    T.c0 = (int)tc * kTC;
+    T.rv = min(kTR, rows - T.r0);
+    T.cv = min(kTC, cols - T.c0);
+    T.first = rem == 0;
+    return T;
   };
 
-  const int64_t t0 = blockIdx.x;
+  // producer: thread 0 arms the stage barrier with the tile's byte count and
+  // issues the four box loads (out-of-range parts are zero-filled), then
+  // forms the slice's encode factor for the consumers.
+  auto issue = [&](uint32_t t, int st) {
+    if (tid == 0 && t < A.ntiles) {
+      const Tile T = tile_of(t);
+      mbar_arrive_expect_tx(&bar[st], kInStage);
+      const int y = (int)(T.e * (uint32_t)rows) + T.r0;
+#pragma unroll
+      for (int j = 0; j < kTC / kBoxC; j++)
+        tma_load_2d(in0 + st * kInStage + j * kBoxBytes, &A.tmap, T.c0 + j * kBoxC, y, &bar[st]);
+      const float am = A.amax[T.e];
+      float G, E;
+      global_scales(am, six_m, G, E);
+      s_E[st] = E;
+      if (T.first) {
+        A.tensor_scale[T.e] = G;
+        if (A.status && !isfinite(am)) atomicOr(A.status, kStatusNonFinite);
+      }
+    }
+  };
+
+  const uint32_t t0 = blockIdx.x;
   issue(t0, 0);
   issue(t0 + gridDim.x, 1);
 
-  int st = 0;
-  for (int64_t t = t0; t < ntiles; t += gridDim.x, st ^= 1) {
-    cp_async_wait<1>();
-    __syncthreads();
-    const int64_t e = t / per_exp;
-    const int rem = (int)(t - e * per_exp);
-    const int tr = rem / tiles_c, tc = rem - tr * tiles_c;
-    const int r0 = tr * kTR, c0 = tc * kTC;
-    const int rv = min(kTR, rows - r0), cv = min(kTC, cols - c0);
-    const float am = amax[e];
-    float G, E;
-    global_scales(am, six_m, G, E);
-    if (tid == 0 && rem == 0) {
-      tensor_scale[e] = G;
-      if (status && !isfinite(am)) atomicOr(status, kStatusNonFinite);
-    }
-    const uint16_t* tile = in0 + st * (kInStage / 2);
+  // rowwise geometry of this thread: 16-column block cb, rows (tid >> 4) + 16k
+  const int cb = tid & 15, rb0 = tid >> 4;
+  const int rbox = (cb >> 2) * kBoxBytes, rchunk = 2 * (cb & 3);
+  // columnwise geometry: row block cr, columns 4q .. 4q+3
+  const int warp = tid >> 5, lane = tid & 31;
+  const int cr = warp >> 1, q = ((warp & 1) << 5) + lane;
+  const int cbox = (q >> 4) * kBoxBytes, cchunk = (q & 15) >> 1, chalf = (q & 1) * 8;
 
-    // rowwise blocks
+  int st = 0;
+  uint32_t it = 0;
+  for (uint32_t t = t0; t < A.ntiles; t += gridDim.x, st ^= 1, it++) {
+    const bool ok = mbar_wait(&bar[st], (it >> 1) & 1, kWaitTries);
+    if (__syncthreads_or(!ok)) {  // a copy never landed: report and stop
+      if (tid == 0 && A.status) atomicOr(A.status, kStatusTimeout);
+      mbar_wait(&bar[st ^ 1], ((it + 1) >> 1) & 1, kWaitTries);
+      return;
+    }
+    const Tile T = tile_of(t);
+    const float E = s_E[st];
+    const unsigned char* tile = in0 + st * kInStage;
+
+    // rowwise blocks: four per thread, 16 rows apart
+    {
+      const int64_t grow0 = (int64_t)T.e * rows + T.r0 + rb0;
+      uint8_t* pc = A.codes_row + grow0 * cols_h + (T.c0 >> 1) + cb * 8;
+      uint8_t* ps = A.scales_row + grow0 * cols_16 + (T.c0 >> 4) + cb;
+      const bool cvalid = cb * 16 < T.cv;
 #pragma unroll 1
-    for (int k = 0; k < 4; k++) {
-      const int b = tid + k * kQT;
-      const int r = b >> 4, cb = b & 15;
-      if (r < rv && cb * 16 < cv) {
-        const uint4 lo = *reinterpret_cast<const uint4*>(tile + r * kTC + swz(2 * cb) * 8);
-        const uint4 hi = *reinterpret_cast<const uint4*>(tile + r * kTC + swz(2 * cb + 1) * 8);
-        const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        uint32_t c0w, c1w, sb;
-        quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
-        const int64_t grow = (int64_t)e * rows + r0 + r;
-        *reinterpret_cast<uint2*>(codes_row + grow * (cols / 2) + c0 / 2 + cb * 8) =
-            make_uint2(c0w, c1w);
-        scales_row[grow * (cols / 16) + c0 / 16 + cb] = (uint8_t)sb;
+      for (int k = 0; k < 4; k++) {
+        const int r = rb0 + 16 * k;
+        if (cvalid && r < T.rv) {
+          const unsigned char* rowp = tile + rbox + r * 128;
+          const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((rchunk ^ (r & 7)) << 4));
+          const uint4 hi = *reinterpret_cast<const uint4*>(rowp + (((rchunk + 1) ^ (r & 7)) << 4));
+          const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          uint32_t c0w, c1w, sb;
+          quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
+          *reinterpret_cast<uint2*>(pc + 16 * k * cols_h) = make_uint2(c0w, c1w);
+          ps[16 * k * cols_16] = (uint8_t)sb;
+        }
       }
     }
 
     if (DUAL) {
-      const int warp = tid >> 5, lane = tid & 31;
-      const int rb = warp >> 1;
-      const int q = ((warp & 1) << 5) + lane;  // columns 4q .. 4q+3 of the tile
-      if (rb * 16 < rv && q * 4 < cv) {
-        const int off = swz(q >> 1) * 8 + (q & 1) * 4;  // element offset within a row
-        uint32_t wc[16];
+      if (cr * 16 < T.rv && q * 4 < T.cv) {
+        const unsigned char* colp = tile + cbox + cr * 16 * 128 + chalf;
+        uint32_t wa[16], wb[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          const uint2 v =
+              *reinterpret_cast<const uint2*>(colp + i * 128 + ((cchunk ^ (i & 7)) << 4));
+          wa[i] = v.x;
+          wb[i] = v.y;
+        }
         uint32_t cj[2], ck[2], sbj, sbk, sw;
-        uint4 outv;
-#pragma unroll
-        for (int i = 0; i < 16; i++)
-          wc[i] = *reinterpret_cast<const uint32_t*>(tile + (rb * 16 + i) * kTC + off);
-        quant_col_pair<F46>(wc, E, tbl, cj, ck, sbj, sbk);
-        outv = make_uint4(cj[0], cj[1], ck[0], ck[1]);
-        *reinterpret_cast<uint4*>(colc + rb * (kTC * 8) + q * 32) = outv;
+        quant_col_pair<F46>(wa, E, tbl, cj, ck, sbj, sbk);
+        *reinterpret_cast<uint4*>(colc + cr * (kTC * 8) + q * 32) =
+            make_uint4(cj[0], cj[1], ck[0], ck[1]);
         sw = sbj | (sbk << 8);
-#pragma unroll
-        for (int i = 0; i < 16; i++)
-          wc[i] = *reinterpret_cast<const uint32_t*>(tile + (rb * 16 + i) * kTC + off + 2);
-        quant_col_pair<F46>(wc, E, tbl, cj, ck, sbj, sbk);
-        outv = make_uint4(cj[0], cj[1], ck[0], ck[1]);
-        *reinterpret_cast<uint4*>(colc + rb * (kTC * 8) + q * 32 + 16) = outv;
+        quant_col_pair<F46>(wb, E, tbl, cj, ck, sbj, sbk);
+        *reinterpret_cast<uint4*>(colc + cr * (kTC * 8) + q * 32 + 16) =
+            make_uint4(cj[0], cj[1], ck[0], ck[1]);
         sw |= (sbj << 16) | (sbk << 24);
-        *reinterpret_cast<uint32_t*>(cols_s + rb * kTC + q * 4) = sw;
+        *reinterpret_cast<uint32_t*>(cols_s + cr * kTC + q * 4) = sw;
       }
     }
     __syncthreads();
-    issue(t + 2 * (int64_t)gridDim.x, st);
+    issue(t + 2 * gridDim.x, st);
 
     if (DUAL) {
       const int c = tid;
-      if (c < cv) {
-        const int nrb = rv >> 4;
-        const int64_t grow = (int64_t)e * cols + c0 + c;
-        uint8_t* dstc = codes_col + grow * (rows / 2) + r0 / 2;
-        uint8_t* dsts = scales_col + grow * (rows / 16) + r0 / 16;
-        for (int rb = 0; rb < nrb; rb++)
-          *reinterpret_cast<uint2*>(dstc + rb * 8) =
-              *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + c * 8);
+      if (c < T.cv) {
+        const int nrb = T.rv >> 4;
+        const int64_t grow = (int64_t)T.e * cols + T.c0 + c;
+        uint8_t* dstc = A.codes_col + grow * rows_h + (T.r0 >> 1);
+        uint8_t* dsts = A.scales_col + grow * rows_16 + (T.r0 >> 4);
+        if (nrb == 4 && (rows & 31) == 0) {
+          const uint2 v0 = *reinterpret_cast<const uint2*>(colc + c * 8);
+          const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + c * 8);
+          const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + c * 8);
+          const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + c * 8);
+          reinterpret_cast<uint4*>(dstc)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+          reinterpret_cast<uint4*>(dstc)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+        } else {
+          for (int rb = 0; rb < nrb; rb++)
+            *reinterpret_cast<uint2*>(dstc + rb * 8) =
+                *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + c * 8);
+        }
         if (nrb == 4 && (rows & 63) == 0) {
-          uint32_t sc = (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
-                        ((uint32_t)cols_s[2 * kTC + c] << 16) |
-                        ((uint32_t)cols_s[3 * kTC + c] << 24);
+          const uint32_t sc = (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
+                              ((uint32_t)cols_s[2 * kTC + c] << 16) |
+                              ((uint32_t)cols_s[3 * kTC + c] << 24);
           *reinterpret_cast<uint32_t*>(dsts) = sc;
         } else {
           for (int rb = 0; rb < nrb; rb++) dsts[rb] = cols_s[rb * kTC + c];
@@ -253,15 +316,10 @@ __global__ void __launch_bounds__(kQT, 2)
       }
     }
   }
-  cp_async_wait<0>();
 }
 
 template <bool F46, bool DUAL>
-static cudaError_t launch_quant_tiles_t(const uint16_t* w, int64_t nexp, int rows, int cols,
-                                        uint8_t* codes_row, uint8_t* scales_row,
-                                        uint8_t* codes_col, uint8_t* scales_col,
-                                        const float* amax, float* tensor_scale, int* status,
-                                        cudaStream_t s) {
+static cudaError_t set_quant_smem() {
   static int attr_done = 0;  // per process; the attribute is per function
   if (!attr_done) {
     cudaError_t err = cudaFuncSetAttribute(k_quant_tiles<F46, DUAL>,
@@ -270,36 +328,57 @@ static cudaError_t launch_quant_tiles_t(const uint16_t* w, int64_t nexp, int row
     if (err != cudaSuccess) return err;
     attr_done = 1;
   }
-  const DevInfo* di = device_info();
-  const int tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
-  const int64_t ntiles = nexp * tiles_r * tiles_c;
-  if (ntiles == 0) return cudaSuccess;
-  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * 2);
-  k_quant_tiles<F46, DUAL><<<grid, kQT, kQuantSmem, s>>>(w, rows, cols, tiles_r, tiles_c, ntiles,
-                                                        codes_row, scales_row, codes_col,
-                                                        scales_col, amax, tensor_scale, status);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
                                uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
                                uint8_t* scales_col, const float* amax, float* tensor_scale,
                                int* status, cudaStream_t s) {
+  const DevInfo* di = device_info();
+  const int tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
+  const int64_t per = (int64_t)tiles_r * tiles_c;
+  const int64_t ntiles = nexp * per;
+  if (ntiles == 0) return cudaSuccess;
+  if (ntiles >= (1ll << 31) - (1ll << 24) || nexp * (int64_t)rows >= (1ll << 31))
+    return cudaErrorInvalidValue;
+  QuantTileArgs A;
+  if (!encode_tmap_2d(&A.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, (uint64_t)cols,
+                      (uint64_t)(nexp * rows), (uint64_t)cols * 2, kBoxC, kTR,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  A.codes_row = codes_row;
+  A.scales_row = scales_row;
+  A.codes_col = codes_col;
+  A.scales_col = scales_col;
+  A.amax = amax;
+  A.tensor_scale = tensor_scale;
+  A.status = status;
+  A.rows = rows;
+  A.cols = cols;
+  A.tiles_c = tiles_c;
+  A.ntiles = (uint32_t)ntiles;
+  A.per_exp.d = (uint32_t)per;
+  make_fastdiv((uint32_t)per, &A.per_exp.m, &A.per_exp.s);
+  A.by_tiles_c.d = (uint32_t)tiles_c;
+  make_fastdiv((uint32_t)tiles_c, &A.by_tiles_c.m, &A.by_tiles_c.s);
+  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * NVQ_QT_MINB);
   const bool dual = codes_col != nullptr;
-  if (f46) {
-    return dual ? launch_quant_tiles_t<true, true>(w, nexp, rows, cols, codes_row, scales_row,
-                                                   codes_col, scales_col, amax, tensor_scale,
-                                                   status, s)
-                : launch_quant_tiles_t<true, false>(w, nexp, rows, cols, codes_row, scales_row,
-                                                    codes_col, scales_col, amax, tensor_scale,
-                                                    status, s);
+  cudaError_t err;
+  if (f46 && dual) {
+    if ((err = set_quant_smem<true, true>())) return err;
+    k_quant_tiles<true, true><<<grid, kQT, kQuantSmem, s>>>(A);
+  } else if (f46) {
+    if ((err = set_quant_smem<true, false>())) return err;
+    k_quant_tiles<true, false><<<grid, kQT, kQuantSmem, s>>>(A);
+  } else if (dual) {
+    if ((err = set_quant_smem<false, true>())) return err;
+    k_quant_tiles<false, true><<<grid, kQT, kQuantSmem, s>>>(A);
+  } else {
+    if ((err = set_quant_smem<false, false>())) return err;
+    k_quant_tiles<false, false><<<grid, kQT, kQuantSmem, s>>>(A);
   }
-  return dual ? launch_quant_tiles_t<false, true>(w, nexp, rows, cols, codes_row, scales_row,
-                                                  codes_col, scales_col, amax, tensor_scale,
-                                                  status, s)
-              : launch_quant_tiles_t<false, false>(w, nexp, rows, cols, codes_row, scales_row,
-                                                   codes_col, scales_col, amax, tensor_scale,
-                                                   status, s);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------ per-token activations
@@ -412,21 +491,21 @@ constexpr int64_t kDqChunk = (int64_t)kDqThreads * kDqPer;  // blocks per item
 
 __global__ void __launch_bounds__(kDqThreads)
     k_dequant(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-              const float* __restrict__ Gs, int64_t blocks_per_slice, int64_t chunks_per_slice,
-              int64_t nitems, uint16_t* __restrict__ dst) {
+              const float* __restrict__ Gs, int64_t blocks_per_slice, FastDiv cps,
+              uint32_t nitems, uint16_t* __restrict__ dst) {
   __shared__ ScaleEnt tbl[128];
   build_scale_table(tbl);
   __syncthreads();
-  for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
-    const int64_t e = it / chunks_per_slice;
-    const int64_t b0 = (it - e * chunks_per_slice) * kDqChunk;
+  for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
+    const uint32_t e = cps.div(it);
+    const int64_t b0 = (int64_t)(it - e * cps.d) * kDqChunk;
     const float G = Gs[e];
     const float2 G2 = make_float2(G, G);
 #pragma unroll
     for (int k = 0; k < kDqPer; k++) {
       const int64_t bl = b0 + k * kDqThreads + threadIdx.x;
       if (bl < blocks_per_slice) {
-        const int64_t b = e * blocks_per_slice + bl;
+        const int64_t b = (int64_t)e * blocks_per_slice + bl;
         const uint2 c = *reinterpret_cast<const uint2*>(codes + b * 8);
         const uint32_t S2 = tbl[scales[b] & 0x7f].negS2 ^ 0x80008000u;
         uint4 o0, o1;
@@ -453,8 +532,12 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
   const int64_t cps = (bps + kDqChunk - 1) / kDqChunk;
   const int64_t nitems = nexp * cps;
   if (nitems == 0) return cudaSuccess;
+  if (nitems >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
+  FastDiv fd;
+  fd.d = (uint32_t)cps;
+  make_fastdiv(fd.d, &fd.m, &fd.s);
   const int grid = (int)std::min<int64_t>(nitems, (int64_t)di->sms * 8);
-  k_dequant<<<grid, kDqThreads, 0, s>>>(codes, scales, G, bps, cps, nitems, dst);
+  k_dequant<<<grid, kDqThreads, 0, s>>>(codes, scales, G, bps, fd, (uint32_t)nitems, dst);
   return cudaGetLastError();
 }
 
@@ -465,24 +548,23 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
 // XOR-swizzled by (row >> 4) & 7 so the writes do not conflict); the tile is
 // then stored as 256-byte runs of the [in, out] bf16 result.
 constexpr int kTqR = 128, kTqC = 256, kTqThreads = 256;
-constexpr int kTqSmem = kTqC * kTqR * 2 + 128 * 16;  // 64 KiB tile + table
+constexpr int kTqSmem = kTqC * kTqR * 2 + kScaleTableBytes;  // 64 KiB tile + table
 
 __global__ void __launch_bounds__(kTqThreads, 3)
     k_dequant_t(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                const float* __restrict__ Gs, int out, int in, int tiles_r, int tiles_c,
-                int64_t ntiles, uint16_t* __restrict__ dst) {
+                const float* __restrict__ Gs, int out, int in, FastDiv per_exp,
+                FastDiv by_tiles_c, uint32_t ntiles, uint16_t* __restrict__ dst) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* const tile = smem;
   ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(smem + kTqC * kTqR * 2);
   build_scale_table(tbl);
   const int tid = threadIdx.x;
   const int g = tid >> 4, b = tid & 15;
-  const int64_t per_exp = (int64_t)tiles_r * tiles_c;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
     __syncthreads();  // table ready / previous tile stored
-    const int64_t e = t / per_exp;
-    const int rem = (int)(t - e * per_exp);
-    const int tr = rem / tiles_c, tc = rem - tr * tiles_c;
+    const uint32_t e = per_exp.div(t);
+    const uint32_t rem = t - e * per_exp.d;
+    const int tr = (int)by_tiles_c.div(rem), tc = (int)(rem - tr * by_tiles_c.d);
     const int r0 = tr * kTqR, c0 = tc * kTqC;
     const int rv = min(kTqR, out - r0), cv = min(kTqC, in - c0);
     const float G = Gs[e];
@@ -544,9 +626,15 @@ cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const 
   const int tiles_r = (out + kTqR - 1) / kTqR, tiles_c = (in + kTqC - 1) / kTqC;
   const int64_t ntiles = nexp * tiles_r * tiles_c;
   if (ntiles == 0) return cudaSuccess;
+  if (ntiles >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
+  FastDiv fpe, ftc;
+  fpe.d = (uint32_t)(tiles_r * tiles_c);
+  make_fastdiv(fpe.d, &fpe.m, &fpe.s);
+  ftc.d = (uint32_t)tiles_c;
+  make_fastdiv(ftc.d, &ftc.m, &ftc.s);
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * 3);
-  k_dequant_t<<<grid, kTqThreads, kTqSmem, s>>>(codes, scales, G, out, in, tiles_r, tiles_c,
-                                                ntiles, dst);
+  k_dequant_t<<<grid, kTqThreads, kTqSmem, s>>>(codes, scales, G, out, in, fpe, ftc,
+                                                (uint32_t)ntiles, dst);
   return cudaGetLastError();
 }
 
