@@ -51,9 +51,7 @@ EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 }  // namespace
 
-bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
-                    uint64_t dim0, uint64_t dim1, uint64_t stride_bytes, uint32_t box0,
-                    uint32_t box1, CUtensorMapSwizzle swizzle) {
+static bool get_encode() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -63,12 +61,32 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     cudaGetLastError();
   });
-  if (!g_encode) return false;
+  return g_encode != nullptr;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t dim0, uint64_t dim1, uint64_t stride_bytes, uint32_t box0,
+                    uint32_t box1, CUtensorMapSwizzle swizzle) {
+  if (!get_encode()) return false;
   const cuuint64_t dims[2] = {dim0, dim1};
   const cuuint64_t strides[1] = {stride_bytes};
   const cuuint32_t box[2] = {box0, box1};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t dim0, uint64_t dim1, uint64_t dim2, uint64_t stride1,
+                    uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2,
+                    CUtensorMapSwizzle swizzle) {
+  if (!get_encode()) return false;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

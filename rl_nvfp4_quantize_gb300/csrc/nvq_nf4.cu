@@ -162,53 +162,61 @@ cudaError_t launch_nf4_quant(const uint16_t* w, int64_t n, uint8_t* codes, float
 // ---------------------------------------------------------------- dequant
 // y = bf16(level[c] * absmax).  A 256-entry table maps a code byte to the
 // pair (level[low nibble], level[high nibble]); one packed multiply and one
-// bf16x2 conversion finish two elements.
+// bf16x2 conversion finish two elements.  The table is replicated 16 times,
+// entry p of copy l at (p * 16 + l) * 8 bytes, and lane l reads copy l & 15:
+// the lanes of a 128-byte wavefront then never share a bank, whatever codes
+// they look up.
 constexpr int kNdThreads = 256;
-constexpr int kNdPer = 4;                                        // units per thread per item
-constexpr int64_t kNdChunk = (int64_t)kNdThreads * kNdPer * 32;  // elements per item
+constexpr int kNdTableBytes = 256 * 16 * 8;  // 32 KiB
+constexpr int kNdSlabs = 8;                   // 8-element slabs per thread per item
+constexpr int64_t kNdChunk = (int64_t)kNdThreads * kNdSlabs * 8;  // elements per item
 
+// Work item = 16384 consecutive elements of one slice.  In slab k, thread t
+// owns elements k*2048 + 8t .. +7: its 4 code bytes, its block's absmax, and
+// a 16-byte output run, so every warp load and store is one contiguous run.
 __global__ void __launch_bounds__(kNdThreads)
     k_nf4_dequant(const uint8_t* __restrict__ codes, const float* __restrict__ absmax,
                   int64_t nexp, int64_t per_slice, FastDiv cps,
                   const int32_t* __restrict__ hit_list, const int32_t* __restrict__ n_hit,
                   uint16_t* __restrict__ dst) {
-  __shared__ float2 pairs[256];
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
-    pairs[i] = make_float2(c_nf4[i & 15], c_nf4[i >> 4]);
+  extern __shared__ __align__(16) float2 pairs[];  // [256][16]
+  for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+    const int p = i >> 4;
+    pairs[i] = make_float2(c_nf4[p & 15], c_nf4[p >> 4]);
+  }
   __syncthreads();
+  const float2* const mine = pairs + (threadIdx.x & 15);
   const uint32_t nslots = hit_list ? (uint32_t)max(0, min(*n_hit, (int32_t)nexp)) : (uint32_t)nexp;
   const uint32_t nitems = nslots * cps.d;
   for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
     const uint32_t slot = cps.div(it);
     const int64_t e = hit_list ? (int64_t)hit_list[slot] : (int64_t)slot;
     if (e < 0 || e >= nexp) continue;
-    const int64_t u0 = (int64_t)(it - slot * cps.d) * (kNdChunk / 32);
-    const int64_t units = per_slice / 32;
+    const int64_t x0 = (int64_t)(it - slot * cps.d) * kNdChunk + threadIdx.x * 8;
     const uint8_t* cs = codes + e * (per_slice / 2);
     const float* as = absmax + e * (per_slice / 64);
     uint16_t* ds = dst + e * per_slice;
+    uint32_t cw[kNdSlabs];
+    float a[kNdSlabs];
 #pragma unroll
-    for (int k = 0; k < kNdPer; k++) {
-      const int64_t u = u0 + k * kNdThreads + threadIdx.x;
-      if (u < units) {
-        const uint4 c = ldg_stream(cs + u * 16);
-        const float a = as[u >> 1];
-        const float2 a2 = make_float2(a, a);
-        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-        uint32_t o[16];
+    for (int k = 0; k < kNdSlabs; k++) {
+      const int64_t x = x0 + k * (kNdThreads * 8);
+      const bool ok = x < per_slice;
+      cw[k] = ok ? __ldg(reinterpret_cast<const uint32_t*>(cs) + (x >> 3)) : 0u;
+      a[k] = ok ? __ldg(as + (x >> 6)) : 0.0f;
+    }
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
+    for (int k = 0; k < kNdSlabs; k++) {
+      const int64_t x = x0 + k * (kNdThreads * 8);
+      if (x < per_slice) {
+        const float2 a2 = make_float2(a[k], a[k]);
+        uint32_t o[4];
 #pragma unroll
-          for (int j = 0; j < 4; j++) {
-            const float2 y = __fmul2_rn(pairs[(cw[i] >> (8 * j)) & 0xff], a2);
-            o[4 * i + j] = bf16x2_rn(y.x, y.y);
-          }
+        for (int j = 0; j < 4; j++) {
+          const float2 y = __fmul2_rn(mine[__byte_perm(cw[k], 0, 0x4440 + j) * 16], a2);
+          o[j] = bf16x2_rn(y.x, y.y);
         }
-        uint4* out = reinterpret_cast<uint4*>(ds + u * 32);
-        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        out[2] = make_uint4(o[8], o[9], o[10], o[11]);
-        out[3] = make_uint4(o[12], o[13], o[14], o[15]);
+        stg_stream(ds + x, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
   }
@@ -224,9 +232,17 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const float* absmax, int64_
   fd.d = (uint32_t)cps;
   make_fastdiv(fd.d, &fd.m, &fd.s);
   const DevInfo* di = device_info();
-  const int grid = (int)std::min<int64_t>(nexp * cps, (int64_t)di->sms * 8);
-  k_nf4_dequant<<<grid, kNdThreads, 0, s>>>(codes, absmax, nexp, per_slice, fd, hit_list, n_hit,
-                                           dst);
+  const int grid = (int)std::min<int64_t>(nexp * cps, (int64_t)di->sms * 6);
+  static int attr_done = 0;
+  if (!attr_done) {
+    cudaError_t err = cudaFuncSetAttribute(k_nf4_dequant,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kNdTableBytes);
+    if (err != cudaSuccess) return err;
+    attr_done = 1;
+  }
+  k_nf4_dequant<<<grid, kNdThreads, kNdTableBytes, s>>>(codes, absmax, nexp, per_slice, fd,
+                                                        hit_list, n_hit, dst);
   return cudaGetLastError();
 }
 

@@ -478,48 +478,69 @@ cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* c
 // --------------------------------------------------------------- dequant
 // y = bf16( (c * S) * G ): c * S formed exactly as an f16 pair, widened to
 // FP32, multiplied by the slice's tensor scale, rounded to bf16.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t byte, uint32_t S2, float2 G2) {
-  const uint32_t h2 = e2m1x2_dec(byte);
-  __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&S2));
-  const float2 y = __fmul2_rn(__half22float2(v), G2);
-  return bf16x2_rn(y.x, y.y);
+// Exact products c*S of an f16 code pair and an f16 scale pair, as FP32
+// (mixed-precision FMA c*S + (-0): the product has at most six significant
+// bits, so nothing is rounded and the sign of zero is kept).
+__device__ __forceinline__ float2 cs_exact(uint32_t h2, uint32_t S2) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 cl, ch, sl, sh;\n\t"
+      "mov.b32 {cl, ch}, %2;\n\t"
+      "mov.b32 {sl, sh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, cl, sl, 0f80000000;\n\t"
+      "fma.rn.f32.f16 %1, ch, sl, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2), "r"(S2));
+  return make_float2(lo, hi);
+}
+
+// Dequantises the 8 codes of a word (one scale S as an f16 pair, tensor
+// scale G): four bf16 pairs, element 2j+{0,1} in word j.
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t S2, float2 G2, uint32_t o[4]) {
+  uint32_t h[4];
+  e2m1x8_dec(w, h);
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const float2 y = __fmul2_rn(cs_exact(h[j], S2), G2);
+    o[j] = bf16x2_rn(y.x, y.y);
+  }
 }
 
 constexpr int kDqThreads = 256;
-constexpr int kDqPer = 4;  // blocks per thread per item
-constexpr int64_t kDqChunk = (int64_t)kDqThreads * kDqPer;  // blocks per item
+constexpr int kDqSlabs = 8;                                     // 8-element slabs per thread
+constexpr int64_t kDqChunk = (int64_t)kDqThreads * kDqSlabs * 8;  // elements per item
 
+// Work item = 16384 consecutive elements of one slice.  In slab k, thread t
+// owns elements k*2048 + 8t .. +7 (half of a block): 4 code bytes, the
+// block's scale byte and a 16-byte output run, so warp accesses are
+// contiguous runs.
 __global__ void __launch_bounds__(kDqThreads)
     k_dequant(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-              const float* __restrict__ Gs, int64_t blocks_per_slice, FastDiv cps,
-              uint32_t nitems, uint16_t* __restrict__ dst) {
+              const float* __restrict__ Gs, int64_t per_slice, FastDiv cps, uint32_t nitems,
+              uint16_t* __restrict__ dst) {
   __shared__ ScaleEnt tbl[128];
   build_scale_table(tbl);
   __syncthreads();
   for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
     const uint32_t e = cps.div(it);
-    const int64_t b0 = (int64_t)(it - e * cps.d) * kDqChunk;
+    const int64_t x0 = (int64_t)(it - e * cps.d) * kDqChunk + threadIdx.x * 8;
+    const int64_t base = (int64_t)e * per_slice;
     const float G = Gs[e];
     const float2 G2 = make_float2(G, G);
+    uint32_t cw[kDqSlabs], sbyte[kDqSlabs];
 #pragma unroll
-    for (int k = 0; k < kDqPer; k++) {
-      const int64_t bl = b0 + k * kDqThreads + threadIdx.x;
-      if (bl < blocks_per_slice) {
-        const int64_t b = (int64_t)e * blocks_per_slice + bl;
-        const uint2 c = *reinterpret_cast<const uint2*>(codes + b * 8);
-        const uint32_t S2 = tbl[scales[b] & 0x7f].negS2 ^ 0x80008000u;
-        uint4 o0, o1;
-        o0.x = dq_pair(c.x & 0xff, S2, G2);
-        o0.y = dq_pair((c.x >> 8) & 0xff, S2, G2);
-        o0.z = dq_pair((c.x >> 16) & 0xff, S2, G2);
-        o0.w = dq_pair(c.x >> 24, S2, G2);
-        o1.x = dq_pair(c.y & 0xff, S2, G2);
-        o1.y = dq_pair((c.y >> 8) & 0xff, S2, G2);
-        o1.z = dq_pair((c.y >> 16) & 0xff, S2, G2);
-        o1.w = dq_pair(c.y >> 24, S2, G2);
-        uint4* out = reinterpret_cast<uint4*>(dst + b * 16);
-        out[0] = o0;
-        out[1] = o1;
+    for (int k = 0; k < kDqSlabs; k++) {
+      const int64_t x = x0 + k * (kDqThreads * 8);
+      const bool ok = x < per_slice;
+      cw[k] = ok ? __ldg(reinterpret_cast<const uint32_t*>(codes) + ((base + x) >> 3)) : 0u;
+      sbyte[k] = ok ? __ldg(scales + ((base + x) >> 4)) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kDqSlabs; k++) {
+      const int64_t x = x0 + k * (kDqThreads * 8);
+      if (x < per_slice) {
+        uint32_t o[4];
+        dq_word(cw[k], pos_s2(tbl[sbyte[k] & 0x7f]), G2, o);
+        stg_stream(dst + base + x, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
   }
@@ -528,8 +549,7 @@ __global__ void __launch_bounds__(kDqThreads)
 cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const float* G,
                            int64_t nexp, int64_t per_slice, uint16_t* dst, cudaStream_t s) {
   const DevInfo* di = device_info();
-  const int64_t bps = per_slice / 16;
-  const int64_t cps = (bps + kDqChunk - 1) / kDqChunk;
+  const int64_t cps = (per_slice + kDqChunk - 1) / kDqChunk;
   const int64_t nitems = nexp * cps;
   if (nitems == 0) return cudaSuccess;
   if (nitems >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
@@ -537,80 +557,114 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
   fd.d = (uint32_t)cps;
   make_fastdiv(fd.d, &fd.m, &fd.s);
   const int grid = (int)std::min<int64_t>(nitems, (int64_t)di->sms * 8);
-  k_dequant<<<grid, kDqThreads, 0, s>>>(codes, scales, G, bps, fd, (uint32_t)nitems, dst);
+  k_dequant<<<grid, kDqThreads, 0, s>>>(codes, scales, G, per_slice, fd, (uint32_t)nitems, dst);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------- transposed dequant
-// Tiles of 128 out-rows x 256 in-columns of the rowwise copy.  Each thread
-// dequantises 8 consecutive out-rows of one 16-wide block column and writes
-// them, transposed, as 16-byte runs into a shared [in][out] tile (chunks
-// XOR-swizzled by (row >> 4) & 7 so the writes do not conflict); the tile is
-// then stored as 256-byte runs of the [in, out] bf16 result.
+// Tiles of 128 out-rows x 256 in-columns of the rowwise copy.  Thread
+// (g = tid & 15, b = tid >> 4) dequantises out-rows 8g .. 8g+7 of 16-wide
+// block column b and writes them, transposed, as 16-byte runs into a shared
+// [in][out] tile laid out as two 128-byte-swizzled TMA boxes of 64 out-rows
+// (chunk c of tile row r at c ^ (r & 7)): the eight lanes of each store
+// phase hit eight different chunks.  One thread then stores the two boxes
+// with TMA into the [nexp, in, out] result (a 3-D map, so a ragged tile never
+// spills into the next slice).  The next tile's codes are loaded into
+// registers while the stores drain.
+#ifndef NVQ_TQ_MINB
+#define NVQ_TQ_MINB 2
+#endif
 constexpr int kTqR = 128, kTqC = 256, kTqThreads = 256;
-constexpr int kTqSmem = kTqC * kTqR * 2 + kScaleTableBytes;  // 64 KiB tile + table
+constexpr int kTqBox = kTqC * 64 * 2;                                  // 32 KiB per box
+constexpr int kTqSmem = 2 * kTqBox + kScaleTableBytes;                  // 64 KiB tile + table
 
-__global__ void __launch_bounds__(kTqThreads, 3)
-    k_dequant_t(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                const float* __restrict__ Gs, int out, int in, FastDiv per_exp,
-                FastDiv by_tiles_c, uint32_t ntiles, uint16_t* __restrict__ dst) {
-  extern __shared__ __align__(128) unsigned char smem[];
+struct __align__(64) DequantTArgs {
+  CUtensorMap tmap;  // dst as [nexp][in][out] bf16, boxes of 64 x 256 x 1
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* G;
+  int out, in;
+  FastDiv per_exp, by_tiles_c;
+  uint32_t ntiles;
+};
+
+__global__ void __launch_bounds__(kTqThreads, NVQ_TQ_MINB) k_dequant_t(const __grid_constant__ DequantTArgs A) {
+  extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* const tile = smem;
-  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(smem + kTqC * kTqR * 2);
+  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(smem + 2 * kTqBox);
   build_scale_table(tbl);
   const int tid = threadIdx.x;
-  const int g = tid >> 4, b = tid & 15;
-  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    __syncthreads();  // table ready / previous tile stored
-    const uint32_t e = per_exp.div(t);
-    const uint32_t rem = t - e * per_exp.d;
-    const int tr = (int)by_tiles_c.div(rem), tc = (int)(rem - tr * by_tiles_c.d);
-    const int r0 = tr * kTqR, c0 = tc * kTqC;
-    const int rv = min(kTqR, out - r0), cv = min(kTqC, in - c0);
-    const float G = Gs[e];
-    const float2 G2 = make_float2(G, G);
-    if (g * 8 < rv && b * 16 < cv) {
-      uint2 cw[8];
-      uint32_t S2[8];
+  const int g = tid & 15, b = tid >> 4;
+  const int out = A.out, in = A.in;
+  const int64_t in_h = in >> 1, in_16 = in >> 4;
+  unsigned char* const box = tile + (g >> 3) * kTqBox;
+
+  struct Tile { uint32_t e; int r0, c0, rv, cv; };
+  auto tile_of = [&](uint32_t t) {
+    Tile T;
+    T.e = A.per_exp.div(t);
+    const uint32_t rem = t - T.e * A.per_exp.d;
+    const int tr = (int)A.by_tiles_c.div(rem), tc = (int)(rem - tr * A.by_tiles_c.d);
+    T.r0 = tr * kTqR;
+    T.c0 = tc * kTqC;
+    T.rv = min(kTqR, out - T.r0);
+    T.cv = min(kTqC, in - T.c0);
+    return T;
+  };
+  uint2 cw[8];
+  uint32_t sb[8];
+  auto load = [&](uint32_t t) {
+    const Tile T = tile_of(t);
+    const bool ok = g * 8 < T.rv && b * 16 < T.cv;
+    const int64_t grow = (int64_t)T.e * out + T.r0 + g * 8;
+    const uint8_t* pc = A.codes + grow * in_h + (T.c0 >> 1) + b * 8;
+    const uint8_t* ps = A.scales + grow * in_16 + (T.c0 >> 4) + b;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      cw[i] = ok ? __ldg(reinterpret_cast<const uint2*>(pc + i * in_h)) : make_uint2(0, 0);
+      sb[i] = ok ? __ldg(ps + i * in_16) : 0u;
+    }
+  };
+
+  if (smem_u32(smem) & 1023u) return;  // the swizzled boxes need a 1 KiB aligned base
+  if (blockIdx.x < A.ntiles) load(blockIdx.x);
+  for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
+    if (tid == 0) bulk_wait_read<0>();  // the previous tile's stores have read the tile
+    __syncthreads();
+    const Tile T = tile_of(t);
+    const float Gv = A.G[T.e];
+    const float2 G2 = make_float2(Gv, Gv);
+    if (g * 8 < T.rv && b * 16 < T.cv) {
+      uint32_t o[8][8];  // o[i][j]: bf16 pair (columns 2j, 2j+1) of row i
 #pragma unroll
       for (int i = 0; i < 8; i++) {
-        const int64_t grow = (int64_t)e * out + r0 + g * 8 + i;
-        cw[i] = *reinterpret_cast<const uint2*>(codes + grow * (in / 2) + c0 / 2 + b * 8);
-        S2[i] = tbl[scales[grow * (in / 16) + c0 / 16 + b] & 0x7f].negS2 ^ 0x80008000u;
+        const uint32_t S2 = pos_s2(tbl[sb[i] & 0x7f]);
+        dq_word(cw[i].x, S2, G2, o[i]);
+        dq_word(cw[i].y, S2, G2, o[i] + 4);
       }
 #pragma unroll
-      for (int kp = 0; kp < 8; kp++) {
-        uint32_t ylo[8], yhi[8];  // bf16 of columns 2kp (low) and 2kp+1 (high) per row i
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const uint32_t word = kp < 4 ? cw[i].x : cw[i].y;
-          const uint32_t byte = (word >> (8 * (kp & 3))) & 0xff;
-          const uint32_t p = dq_pair(byte, S2[i], G2);
-          ylo[i] = p & 0xffffu;
-          yhi[i] = p >> 16;
-        }
-        const int rowA = b * 16 + 2 * kp, rowB = rowA + 1;  // in-index within the tile
-        const int chA = g ^ ((rowA >> 4) & 7), chB = g ^ ((rowB >> 4) & 7);
-        uint4 va = make_uint4(ylo[0] | (ylo[1] << 16), ylo[2] | (ylo[3] << 16),
-                              ylo[4] | (ylo[5] << 16), ylo[6] | (ylo[7] << 16));
-        uint4 vb = make_uint4(yhi[0] | (yhi[1] << 16), yhi[2] | (yhi[3] << 16),
-                              yhi[4] | (yhi[5] << 16), yhi[6] | (yhi[7] << 16));
-        *reinterpret_cast<uint4*>(tile + rowA * (kTqR * 2) + chA * 16) = va;
-        *reinterpret_cast<uint4*>(tile + rowB * (kTqR * 2) + chB * 16) = vb;
+      for (int j = 0; j < 8; j++) {
+        const int r = b * 16 + 2 * j;  // tile row (in-index) of column 2j
+        const int off0 = r * 128 + (((g & 7) ^ (r & 7)) << 4);
+        const int off1 = (r + 1) * 128 + (((g & 7) ^ ((r + 1) & 7)) << 4);
+        *reinterpret_cast<uint4*>(box + off0) =
+            make_uint4(__byte_perm(o[0][j], o[1][j], 0x5410), __byte_perm(o[2][j], o[3][j], 0x5410),
+                       __byte_perm(o[4][j], o[5][j], 0x5410), __byte_perm(o[6][j], o[7][j], 0x5410));
+        *reinterpret_cast<uint4*>(box + off1) =
+            make_uint4(__byte_perm(o[0][j], o[1][j], 0x7632), __byte_perm(o[2][j], o[3][j], 0x7632),
+                       __byte_perm(o[4][j], o[5][j], 0x7632), __byte_perm(o[6][j], o[7][j], 0x7632));
       }
     }
+    fence_proxy_async_smem();  // make this thread's tile writes visible to the TMA unit
     __syncthreads();
-#pragma unroll 4
-    for (int it = 0; it < (kTqC * kTqR * 2 / 16) / kTqThreads; it++) {
-      const int lin = it * kTqThreads + tid;
-      const int row = lin >> 4, j = lin & 15;  // in-row within tile, 16-byte chunk
-      if (row < cv && j * 8 < rv) {
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + row * (kTqR * 2) +
-                                                        (j ^ ((row >> 4) & 7)) * 16);
-        *reinterpret_cast<uint4*>(dst + ((int64_t)e * in + c0 + row) * out + r0 + j * 8) = v;
-      }
+    if (tid == 0) {
+      tma_store_3d(&A.tmap, T.r0, T.c0, (int)T.e, tile);
+      if (T.rv > 64) tma_store_3d(&A.tmap, T.r0 + 64, T.c0, (int)T.e, tile + kTqBox);
+      bulk_commit();
     }
+    if (t + gridDim.x < A.ntiles) load(t + gridDim.x);
   }
+  if (tid == 0) bulk_wait<0>();
 }
 
 cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const float* G,
@@ -626,15 +680,24 @@ cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const 
   const int tiles_r = (out + kTqR - 1) / kTqR, tiles_c = (in + kTqC - 1) / kTqC;
   const int64_t ntiles = nexp * tiles_r * tiles_c;
   if (ntiles == 0) return cudaSuccess;
-  if (ntiles >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
-  FastDiv fpe, ftc;
-  fpe.d = (uint32_t)(tiles_r * tiles_c);
-  make_fastdiv(fpe.d, &fpe.m, &fpe.s);
-  ftc.d = (uint32_t)tiles_c;
-  make_fastdiv(ftc.d, &ftc.m, &ftc.s);
-  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * 3);
-  k_dequant_t<<<grid, kTqThreads, kTqSmem, s>>>(codes, scales, G, out, in, fpe, ftc,
-                                                (uint32_t)ntiles, dst);
+  if (ntiles >= (1ll << 31) - (1ll << 24) || nexp >= (1ll << 31)) return cudaErrorInvalidValue;
+  DequantTArgs A;
+  if (!encode_tmap_3d(&A.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, dst, (uint64_t)out, (uint64_t)in,
+                      (uint64_t)nexp, (uint64_t)out * 2, (uint64_t)out * in * 2, 64, kTqC, 1,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  A.codes = codes;
+  A.scales = scales;
+  A.G = G;
+  A.out = out;
+  A.in = in;
+  A.per_exp.d = (uint32_t)(tiles_r * tiles_c);
+  make_fastdiv(A.per_exp.d, &A.per_exp.m, &A.per_exp.s);
+  A.by_tiles_c.d = (uint32_t)tiles_c;
+  make_fastdiv(A.by_tiles_c.d, &A.by_tiles_c.m, &A.by_tiles_c.s);
+  A.ntiles = (uint32_t)ntiles;
+  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * NVQ_TQ_MINB);
+  k_dequant_t<<<grid, kTqThreads, kTqSmem, s>>>(A);
   return cudaGetLastError();
 }
 
