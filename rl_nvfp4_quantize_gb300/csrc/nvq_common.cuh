@@ -38,6 +38,14 @@ __device__ __forceinline__ uint32_t maxabs2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Per half: max(|a|, |b|), a NaN in either operand giving NaN (sign bits of
+// the result are meaningless).
+__device__ __forceinline__ uint32_t maxabs2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Per half: unsigned 16-bit max of the magnitude bits.  NaN patterns compare
 // above infinity, so a NaN anywhere propagates to the result.
 __device__ __forceinline__ uint32_t umaxmag2(uint32_t m, uint32_t w) {

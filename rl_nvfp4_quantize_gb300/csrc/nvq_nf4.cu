@@ -106,15 +106,17 @@ __global__ void __launch_bounds__(kNqThreads)
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) v[u] = act ? ldg_stream(w + h * 32 + u * 8) : make_uint4(0, 0, 0, 0);
-    uint32_t m = 0;
+    uint32_t m = maxabs2_nan(v[0].x, v[0].y);
+    m = maxabs2_nan(m, v[0].z);
+    m = maxabs2_nan(m, v[0].w);
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      m = umaxmag2(m, v[u].x);
-      m = umaxmag2(m, v[u].y);
-      m = umaxmag2(m, v[u].z);
-      m = umaxmag2(m, v[u].w);
+    for (int u = 1; u < 4; u++) {
+      m = maxabs2_nan(m, v[u].x);
+      m = maxabs2_nan(m, v[u].y);
+      m = maxabs2_nan(m, v[u].z);
+      m = maxabs2_nan(m, v[u].w);
     }
-    uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
+    uint32_t mm = maxabs2_nan(m, __byte_perm(m, 0, 0x1032)) & 0x7fff0000u;  // FP32 bits
     mm = max(mm, __shfl_xor_sync(0xffffffffu, mm, 1));
     const float am = __uint_as_float(mm);
     const float r = (am == 0.0f) ? 0.0f : __frcp_rn(am);
@@ -124,14 +126,17 @@ __global__ void __launch_bounds__(kNqThreads)
 #pragma unroll
       for (int u = 0; u < 4; u++) {
         const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t o = 0;
+        uint32_t c[8];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-          const float2 x = __fmul2_rn(make_float2(lo_f(wv[i]), hi_f(wv[i])), r2);
-          const uint32_t b = nf4_code(x.x, tbl) | (nf4_code(x.y, tbl) << 4);
-          o |= b << (8 * i);
+          const float2 x = __fmul2_rn(widen2(wv[i]), r2);
+          c[2 * i] = nf4_code(x.x, tbl);
+          c[2 * i + 1] = nf4_code(x.y, tbl);
         }
-        out[u] = o;
+        // nibble j of the word is code j (a shallow tree keeps the chain short)
+        const uint32_t b0 = c[0] | (c[1] << 4), b1 = c[2] | (c[3] << 4);
+        const uint32_t b2 = c[4] | (c[5] << 4), b3 = c[6] | (c[7] << 4);
+        out[u] = (b0 | (b1 << 8)) | ((b2 | (b3 << 8)) << 16);
       }
       *reinterpret_cast<uint4*>(codes + h * 16) = make_uint4(out[0], out[1], out[2], out[3]);
       if ((h & 1) == 0) {
