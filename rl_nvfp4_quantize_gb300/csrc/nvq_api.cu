@@ -225,14 +225,12 @@ int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, 
   if ((rc = device_check())) return rc;
   cudaStream_t s = cs(stream);
   const bool f46 = flags & NVQ_4OVER6;
-  if (!(flags & NVQ_AMAX_GIVEN)) {
-    if ((rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
-    if (total > 0 && (rc = launch_result(nvq::launch_amax(w, nexp, rows * cols, amax, s))))
-      return rc;
-  }
+  const bool given = flags & NVQ_AMAX_GIVEN;
+  if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
   if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
   return launch_result(nvq::launch_quant_tiles(w, nexp, (int)rows, (int)cols, f46, codes, scales,
-                                               nullptr, nullptr, amax, tensor_scale, status, s));
+                                               nullptr, nullptr, amax, tensor_scale, status,
+                                               !given, s));
 }
 
 int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in, unsigned flags,
@@ -257,14 +255,12 @@ int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in
   if ((rc = device_check())) return rc;
   cudaStream_t s = cs(stream);
   const bool f46 = flags & NVQ_4OVER6;
-  if (!(flags & NVQ_AMAX_GIVEN)) {
-    if ((rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
-    if (total > 0 && (rc = launch_result(nvq::launch_amax(w, nexp, out * in, amax, s)))) return rc;
-  }
+  const bool given = flags & NVQ_AMAX_GIVEN;
+  if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
   if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
   return launch_result(nvq::launch_quant_tiles(w, nexp, (int)out, (int)in, f46, codes_row,
                                                scales_row, codes_col, scales_col, amax,
-                                               tensor_scale, status, s));
+                                               tensor_scale, status, !given, s));
 }
 
 int nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,

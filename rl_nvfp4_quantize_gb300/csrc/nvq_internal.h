@@ -51,10 +51,13 @@ cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, floa
                         cudaStream_t s);
 
 // Rowwise (and, with codes_col != nullptr, columnwise) NVFP4 of a stack.
+// With compute_amax the per-slice amax (zeroed by the caller) is reduced
+// here: the first chunk of slices by a reduction pass, every later chunk
+// inside the launch that quantises the chunk before it.
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
                                uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
-                               uint8_t* scales_col, const float* amax, float* tensor_scale,
-                               int* status, cudaStream_t s);
+                               uint8_t* scales_col, float* amax, float* tensor_scale,
+                               int* status, bool compute_amax, cudaStream_t s);
 
 cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* codes,
                        uint8_t* scales, float* token_scale, int* status, cudaStream_t s);

@@ -9,6 +9,7 @@
 #include <cfloat>
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 
 #include "nvq_common.cuh"
 #include "nvq_internal.h"
@@ -137,14 +138,19 @@ struct __align__(64) QuantTileArgs {
   uint8_t* scales_row;
   uint8_t* codes_col;
   uint8_t* scales_col;
-  const float* amax;
+  const float* amax;      // complete for this launch's slices
   float* tensor_scale;
   int* status;
   int rows, cols;         // per slice
   int tiles_c;            // column tiles per slice
-  uint32_t ntiles;        // all slices
+  uint32_t ntiles;        // tiles of this launch
   FastDiv per_exp;        // tiles per slice
   FastDiv by_tiles_c;
+  uint32_t e0;            // first slice of this launch
+  uint32_t nexp;          // slices in the whole stack
+  uint32_t ahead;         // > 0: also reduce the amax of slice e + ahead (0: off)
+  const uint16_t* w;      // the stack (for the look-ahead amax reads)
+  float* amax_out;        // the look-ahead amax accumulators (same array as amax)
 };
 
 template <bool F46, bool DUAL>
@@ -179,8 +185,9 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
   struct Tile { uint32_t e; int r0, c0, rv, cv; bool first; };
   auto tile_of = [&](uint32_t t) {
     Tile T;
-    T.e = A.per_exp.div(t);
-    const uint32_t rem = t - T.e * A.per_exp.d;
+    const uint32_t el = A.per_exp.div(t);
+    const uint32_t rem = t - el * A.per_exp.d;
+    T.e = A.e0 + el;
     const uint32_t tr = A.by_tiles_c.div(rem);
     const uint32_t tc = rem - tr * (uint32_t)A.tiles_c;
     T.r0 = (int)tr * kTR;
@@ -238,6 +245,26 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
     const float E = s_E[st];
     const unsigned char* tile = in0 + st * kInStage;
 
+    // look-ahead amax: the same tile position of slice e + ahead is read now
+    // and reduced after the rowwise pass, whose arithmetic covers the load
+    // latency (the dual kernel is bound by instruction issue, so these reads
+    // use HBM bandwidth it leaves idle).
+    const bool ahead = DUAL && A.ahead != 0 && T.e + A.ahead < A.nexp;
+    uint32_t sh[4][8];
+    if (ahead) {
+      const uint16_t* base = A.w + ((int64_t)(T.e + A.ahead) * rows + T.r0) * cols + T.c0;
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const int id = tid + i * kQT, r = id >> 4, c = (id & 15) * 16;
+        if (r < T.rv && c < T.cv) {
+          ldg32(base + (int64_t)r * cols + c, sh[i]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; k++) sh[i][k] = 0;
+        }
+      }
+    }
+
     // rowwise blocks: four per thread, 16 rows apart
     {
       const int64_t grow0 = (int64_t)T.e * rows + T.r0 + rb0;
@@ -258,6 +285,18 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
           ps[16 * k * cols_16] = (uint8_t)sb;
         }
       }
+    }
+
+    if (ahead) {
+      uint32_t m = maxabs2_nan(sh[0][0], sh[0][1]);
+#pragma unroll
+      for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+          if (i > 0 || k > 1) m = maxabs2_nan(m, sh[i][k]);
+      uint32_t mm = maxabs2_nan(m, __byte_perm(m, 0, 0x1032)) & 0x7fff0000u;  // FP32 bits
+      mm = __reduce_max_sync(0xffffffffu, mm);
+      if ((tid & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(A.amax_out + T.e + A.ahead), mm);
     }
 
     if (DUAL) {
@@ -333,8 +372,8 @@ static cudaError_t set_quant_smem() {
 
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
                                uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
-                               uint8_t* scales_col, const float* amax, float* tensor_scale,
-                               int* status, cudaStream_t s) {
+                               uint8_t* scales_col, float* amax, float* tensor_scale,
+                               int* status, bool compute_amax, cudaStream_t s) {
   const DevInfo* di = device_info();
   const int tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
   const int64_t per = (int64_t)tiles_r * tiles_c;
@@ -352,33 +391,64 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
   A.codes_col = codes_col;
   A.scales_col = scales_col;
   A.amax = amax;
+  A.amax_out = amax;
   A.tensor_scale = tensor_scale;
   A.status = status;
   A.rows = rows;
   A.cols = cols;
   A.tiles_c = tiles_c;
-  A.ntiles = (uint32_t)ntiles;
   A.per_exp.d = (uint32_t)per;
   make_fastdiv((uint32_t)per, &A.per_exp.m, &A.per_exp.s);
   A.by_tiles_c.d = (uint32_t)tiles_c;
   make_fastdiv((uint32_t)tiles_c, &A.by_tiles_c.m, &A.by_tiles_c.s);
-  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * NVQ_QT_MINB);
+  A.nexp = (uint32_t)nexp;
+  A.w = w;
+  const int full_grid = di->sms * NVQ_QT_MINB;
+  // Slices per launch: with the look-ahead amax every launch quantises one
+  // chunk while reducing the amax of the next, so each launch must see its
+  // chunk's amax complete.  A chunk covers about 40 waves of tiles, so the
+  // partial last wave of each launch costs little.
+  // The look-ahead is used by the dual-layout kernel only (the rowwise kernel
+  // is close to memory bound, where a separate reduction pass is as fast);
+  // its reads are 32-byte vectors, so it also needs a 32-byte aligned stack.
+  // Otherwise the whole amax is reduced by one pass up front.
+  const bool lookahead = compute_amax && codes_col != nullptr &&
+                         (reinterpret_cast<uintptr_t>(w) & 31) == 0;
+  int64_t chunk = nexp;
+  if (lookahead) {
+    chunk = std::max<int64_t>(1, (40ll * full_grid + per - 1) / per);
+    // NVQ_QUANT_CHUNK (slices per launch) overrides the choice; the tests use
+    // it to exercise the look-ahead on small stacks.
+    if (const char* env = std::getenv("NVQ_QUANT_CHUNK")) {
+      const long long v = std::atoll(env);
+      if (v > 0) chunk = v;
+    }
+    chunk = std::min<int64_t>(chunk, nexp);
+  }
+  if (compute_amax) {
+    cudaError_t err = launch_amax(w, chunk, (int64_t)rows * cols, amax, s);
+    if (err != cudaSuccess) return err;
+  }
   const bool dual = codes_col != nullptr;
   cudaError_t err;
-  if (f46 && dual) {
-    if ((err = set_quant_smem<true, true>())) return err;
-    k_quant_tiles<true, true><<<grid, kQT, kQuantSmem, s>>>(A);
-  } else if (f46) {
-    if ((err = set_quant_smem<true, false>())) return err;
-    k_quant_tiles<true, false><<<grid, kQT, kQuantSmem, s>>>(A);
-  } else if (dual) {
-    if ((err = set_quant_smem<false, true>())) return err;
-    k_quant_tiles<false, true><<<grid, kQT, kQuantSmem, s>>>(A);
-  } else {
-    if ((err = set_quant_smem<false, false>())) return err;
-    k_quant_tiles<false, false><<<grid, kQT, kQuantSmem, s>>>(A);
+  if (f46 && dual) err = set_quant_smem<true, true>();
+  else if (f46) err = set_quant_smem<true, false>();
+  else if (dual) err = set_quant_smem<false, true>();
+  else err = set_quant_smem<false, false>();
+  if (err != cudaSuccess) return err;
+  for (int64_t e0 = 0; e0 < nexp; e0 += chunk) {
+    const int64_t n = std::min<int64_t>(chunk, nexp - e0);
+    A.e0 = (uint32_t)e0;
+    A.ntiles = (uint32_t)(n * per);
+    A.ahead = (lookahead && e0 + chunk < nexp) ? (uint32_t)chunk : 0u;
+    const int grid = (int)std::min<int64_t>(n * per, full_grid);
+    if (f46 && dual) k_quant_tiles<true, true><<<grid, kQT, kQuantSmem, s>>>(A);
+    else if (f46) k_quant_tiles<true, false><<<grid, kQT, kQuantSmem, s>>>(A);
+    else if (dual) k_quant_tiles<false, true><<<grid, kQT, kQuantSmem, s>>>(A);
+    else k_quant_tiles<false, false><<<grid, kQT, kQuantSmem, s>>>(A);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------ per-token activations

@@ -214,3 +214,39 @@ def test_stream_ordering_on_side_stream(nvq, oracle_mod):
     s.synchronize()
     o = oracle_mod.nvfp4_quantize(u16(w), four_over_six=True)
     assert_same(u16(dt), oracle_mod.nvfp4_dequant_t(o["codes"], o["scales"], o["G"], 128, 512))
+
+
+@pytest.mark.parametrize("chunk", ["1", "2", "3"])
+@pytest.mark.parametrize("shape", [(7, 80, 336), (5, 64, 256), (4, 144, 528)])
+def test_lookahead_amax_chunks(nvq, oracle_mod, shape, chunk, monkeypatch):
+    """Slices quantised in chunks, each launch reducing the next chunk's amax
+    while it quantises the current one: outputs are those of the oracle."""
+    monkeypatch.setenv("NVQ_QUANT_CHUNK", chunk)
+    w = weights(shape, seed=300 + int(chunk) + sum(shape))
+    wn = u16(w)
+    for f46 in (False, True):
+        r = nvq.nvfp4_quantize_dual(w.cuda(), four_over_six=f46)
+        orow = oracle_mod.nvfp4_quantize(wn, four_over_six=f46)
+        ocol = oracle_mod.nvfp4_quantize_colwise(wn, four_over_six=f46)
+        assert_same(f32(r["amax"]).view(np.uint32), orow["amax"].view(np.uint32), "amax")
+        assert_same(f32(r["tensor_scale"]).view(np.uint32), orow["G"].view(np.uint32), "G")
+        assert_same(u8(r["codes_row"]), orow["codes"], "codes_row")
+        assert_same(u8(r["scales_row"]), orow["scales"], "scales_row")
+        assert_same(u8(r["codes_col"]), ocol["codes"], "codes_col")
+        assert_same(u8(r["scales_col"]), ocol["scales"], "scales_col")
+        r1 = nvq.nvfp4_quantize(w.cuda(), four_over_six=f46)
+        assert_same(u8(r1["codes"]), orow["codes"], "rowwise-only codes")
+
+
+def test_misaligned_stack_falls_back(nvq, oracle_mod, monkeypatch):
+    """A stack that is 16- but not 32-byte aligned takes the separate amax pass."""
+    monkeypatch.setenv("NVQ_QUANT_CHUNK", "1")
+    w = weights((3, 64, 256), seed=77)
+    buf = torch.empty(w.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    wv = buf[8:].view(3, 64, 256)
+    wv.copy_(w.cuda())
+    assert wv.data_ptr() % 32 == 16
+    r = nvq.nvfp4_quantize_dual(wv, four_over_six=True)
+    o = oracle_mod.nvfp4_quantize(u16(w), four_over_six=True)
+    assert_same(u8(r["codes_row"]), o["codes"], "codes_row")
+    assert_same(f32(r["amax"]).view(np.uint32), o["amax"].view(np.uint32), "amax")
