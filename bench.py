@@ -97,15 +97,25 @@ class Workload:
 
     def calls(self):
         """(name, callable, algorithmic bytes, kernel launches) for one step."""
+        import torch
         import rl_nvfp4_quantize_gb300 as nvq
         n_gu = GATE_UP[0] * GATE_UP[1] * GATE_UP[2]
         n_dn = DOWN[0] * DOWN[1] * DOWN[2]
+        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+
+        def dual_launches(E, R, K):
+            # one zeroing of amax, one amax pass over the first chunk, then one
+            # tile launch per chunk of slices (about 40 waves of 64 x 256 tiles
+            # over two CTAs per SM); checked against the ncu launch list
+            per = -(-R // 64) * -(-K // 256)
+            chunk = min(E, max(1, -(-40 * 2 * sms // per)))
+            return 2 + -(-E // chunk)
         L = []
         for name, w, q, n, E in (("nvfp4_quantize_dual[gate_up]", self.gu, self.q_gu, n_gu, GATE_UP[0]),
                                  ("nvfp4_quantize_dual[down]", self.dn, self.q_dn, n_dn, DOWN[0])):
             L.append((name, (lambda w=w, q=q: nvq.nvfp4_quantize_dual(
                 w, four_over_six=True, status=self.status, out=q)),
-                2 * n + 2 * nvfp4_bytes(n) + 8 * E, 3))
+                2 * n + 2 * nvfp4_bytes(n) + 8 * E, dual_launches(*w.shape)))
         for name, q, dst, n, E in (("nvfp4_dequant_t[gate_up]", self.q_gu, self.dqt_gu, n_gu, GATE_UP[0]),
                                    ("nvfp4_dequant_t[down]", self.q_dn, self.dqt_dn, n_dn, DOWN[0])):
             L.append((name, (lambda q=q, dst=dst: nvq.nvfp4_dequant_t(
@@ -292,16 +302,22 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def setup_dist(args):
+def setup_dist(args, backend="nccl"):
+    """Rank, world size and local rank from the torchrun environment; with
+    more than one rank, joins the process group (NCCL on the GPU machine; the
+    host tests use gloo) and selects this rank's GPU."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -313,13 +329,22 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """The largest value of v over all ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(world, bytes_per_step, steps, elapsed_max):
+    """Whole-job GB/s: every rank runs the same step on its own GPU (weak
+    scaling), so the job moves world * bytes_per_step per step, and the job
+    takes as long as its slowest rank."""
+    return world * bytes_per_step * steps / elapsed_max / 1e9
 
 
 def main():
@@ -390,7 +415,7 @@ def main():
     elapsed = t_start.elapsed_time(t_end) / 1e3
     elapsed_max = max_over_ranks(world, elapsed)
     ms_step = 1e3 * elapsed_max / args.steps
-    value = world * step_bytes * args.steps / elapsed_max / 1e9
+    value = job_rate(world, step_bytes, args.steps, elapsed_max)
 
     per_call = []
     for j, (name, _, b, k) in enumerate(calls):
@@ -491,7 +516,7 @@ def measure_e2e(wl, calls, steps, stream, world):
     b.record(stream)
     torch.cuda.synchronize()
     el = max_over_ranks(world, a.elapsed_time(b) / 1e3)
-    return {"value": round(world * step_bytes * steps / el / 1e9, 3), "unit": "GB/s",
+    return {"value": round(job_rate(world, step_bytes, steps, el), 3), "unit": "GB/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "ms_per_step": round(1e3 * el / steps, 3)}
 

@@ -34,8 +34,10 @@
  *  - Device status word.  `status` (nullable, device int) receives, by
  *    atomic OR, data-dependent conditions found while the kernels run:
  *    NVQ_STATUS_NONFINITE when an amax / absmax is NaN or infinite (those
- *    outputs are then unspecified) and NVQ_STATUS_BAD_INDEX when a router
- *    index lies outside [0, nexp) (the index is ignored).  Kernels never trap.
+ *    outputs are then unspecified), NVQ_STATUS_BAD_INDEX when a router
+ *    index lies outside [0, nexp) (the index is ignored) and
+ *    NVQ_STATUS_TIMEOUT when a bounded internal wait gave up.  Kernels never
+ *    trap and never spin without a bound.
  *  - Calls on different streams that write the same buffers race; the
  *    library is otherwise thread-safe (it has no global mutable state).
  */
@@ -82,8 +84,14 @@ enum nvq_flags {
 
 /* Bits of the device status word. */
 enum nvq_device_status {
-  NVQ_STATUS_NONFINITE = 1,
-  NVQ_STATUS_BAD_INDEX = 2
+  NVQ_STATUS_NONFINITE = 1, /* an amax / absmax is NaN or infinite           */
+  NVQ_STATUS_BAD_INDEX = 2, /* a router index outside [0, nexp) was ignored  */
+  /* An internal wait (a bulk tile copy that did not arrive within a fixed
+     number of polls, or a shared-memory layout the kernel could not align)
+     was abandoned: the CTA stopped early and some outputs of the call were
+     not written.  Never expected in normal operation; the call's outputs are
+     then unspecified and the device stays usable. */
+  NVQ_STATUS_TIMEOUT = 4
 };
 
 /* Library version, (major << 16) | minor. */

@@ -22,7 +22,7 @@ import os
 import torch
 
 __all__ = [
-    "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX",
+    "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
     "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t",
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed",
     "nf4_codebook", "debug_convert", "lib", "library_path",
@@ -32,6 +32,7 @@ FLAG_4OVER6 = 1
 FLAG_AMAX_GIVEN = 2
 STATUS_NONFINITE = 1
 STATUS_BAD_INDEX = 2
+STATUS_TIMEOUT = 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libnvq.so")
