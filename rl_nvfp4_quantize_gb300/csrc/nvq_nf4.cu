@@ -36,56 +36,55 @@ void nf4_levels_host(float out[16]) {
 }
 
 // --------------------------------------------------------------- quantise
-// The nearest level is found through a lookup on the top 12 bits of the
-// normalised value v (sign, exponent, 3 mantissa bits).  Each such bucket
-// spans at most one eighth of an octave, and consecutive NF4 midpoints are
-// further apart than that, so a bucket holds at most one midpoint mu: the
-// code is lo + (v > mu), lo being the number of midpoints below the bucket.
-// With mu = +inf for buckets without a midpoint this reproduces exactly
-// "the number of midpoints strictly below v".
+// The nearest level is found through the cell of g = fl(16 v + 96): for every
+// |v| < 2, g lies in [64, 128), where floats step by 2^-17, so bits 17..22 of
+// g number 64 cells of width 1/16 in v.  g never decreases as v grows, and the
+// NF4 midpoints lie more than 1/16 apart, so a cell holds at most one midpoint
+// mu; the code, the number of midpoints strictly below v, is then
+// lo + (v > mu), with lo the number of midpoints in lower cells and mu = +inf
+// in cells without one.  Any float (a NaN or an infinity too) lands in one of
+// the 64 cells.  The 64-entry table is replicated for the 32 lanes (row of
+// cell c at byte 256 c, lane l at byte 8 l): every lookup of a warp touches
+// each bank pair once, whatever cells its lanes hit.
 struct __align__(8) Nf4Ent {
   float thr;
   int lo;
 };
-constexpr int kNf4Buckets = 4096;
+constexpr int kNf4Cells = 64;
 constexpr int kNqThreads = 256;
-constexpr int kNqSmem = kNf4Buckets * 8;
+constexpr int kNqSmem = kNf4Cells * 32 * 8;
 
-__device__ __forceinline__ void build_nf4_buckets(Nf4Ent* tbl) {
+// Byte offset of the table row of the cell of g.
+__device__ __forceinline__ uint32_t nf4_cell_row(float g) {
+  return (__float_as_uint(g) >> 9) & ((uint32_t)(kNf4Cells - 1) << 8);
+}
+
+__device__ __forceinline__ void build_nf4_cells(Nf4Ent* tbl) {
   float m[15];
+  uint32_t cm[15];
 #pragma unroll
-  for (int j = 0; j < 15; j++) m[j] = __fmul_rn(__fadd_rn(c_nf4[j], c_nf4[j + 1]), 0.5f);
-  for (int idx = threadIdx.x; idx < kNf4Buckets; idx += blockDim.x) {
-    const uint32_t key = (uint32_t)idx & 0x7ffu;
-    const bool neg = (idx >> 11) != 0;
+  for (int j = 0; j < 15; j++) {
+    m[j] = __fmul_rn(__fadd_rn(c_nf4[j], c_nf4[j + 1]), 0.5f);
+    cm[j] = nf4_cell_row(__fmaf_rn(m[j], 16.0f, 96.0f)) >> 8;
+  }
+  for (int idx = threadIdx.x; idx < kNf4Cells * 32; idx += blockDim.x) {
+    const uint32_t cell = (uint32_t)idx >> 5;
     Nf4Ent ent;
     ent.thr = __int_as_float(0x7f800000);
     ent.lo = 0;
-    if (key < 0x7f8u) {  // finite magnitudes only
-      const float L = __uint_as_float(key << 20), U = __uint_as_float((key + 1) << 20);
-      int lo = 0;
-      if (!neg) {  // v in [L, U)
 #pragma unroll
-        for (int j = 0; j < 15; j++) {
-          if (m[j] < L) lo++;
-          else if (m[j] < U) ent.thr = m[j];
-        }
-      } else {  // v in (-U, -L]
-#pragma unroll
-        for (int j = 0; j < 15; j++) {
-          if (m[j] <= -U) lo++;
-          else if (m[j] <= -L) ent.thr = m[j];
-        }
-      }
-      ent.lo = lo;
+    for (int j = 0; j < 15; j++) {
+      if (cm[j] < cell) ent.lo++;
+      else if (cm[j] == cell) ent.thr = m[j];
     }
     tbl[idx] = ent;
   }
 }
 
-__device__ __forceinline__ uint32_t nf4_code(float v, const Nf4Ent* tbl) {
-  const Nf4Ent e = tbl[__float_as_uint(v) >> 20];
-  return (uint32_t)(e.lo + (v > e.thr ? 1 : 0));
+// Code of v; g = fl(16 v + 96); `lane_tbl` is this lane's column of the table.
+__device__ __forceinline__ uint32_t nf4_code(float v, float g, const unsigned char* lane_tbl) {
+  const Nf4Ent e = *reinterpret_cast<const Nf4Ent*>(lane_tbl + nf4_cell_row(g));
+  return (uint32_t)e.lo + (v > e.thr ? 1u : 0u);
 }
 
 // One thread per half block (32 elements = 64 bytes); the two halves of a
@@ -94,10 +93,11 @@ __global__ void __launch_bounds__(kNqThreads)
     k_nf4_quant(const uint16_t* __restrict__ w, int64_t nhalf, uint8_t* __restrict__ codes,
                 float* __restrict__ absmax, int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  Nf4Ent* const tbl = reinterpret_cast<Nf4Ent*>(smem);
-  build_nf4_buckets(tbl);
+  build_nf4_cells(reinterpret_cast<Nf4Ent*>(smem));
   __syncthreads();
+  const unsigned char* const lane_tbl = smem + (threadIdx.x & 31) * 8;
   const int64_t stride = (int64_t)gridDim.x * kNqThreads;
+  const float2 k16 = make_float2(16.0f, 16.0f), k96 = make_float2(96.0f, 96.0f);
   // The loop bound is taken at the warp's first lane so that whole warps
   // stay together for the shuffle; lanes past the end only skip the stores.
   for (int64_t h = (int64_t)blockIdx.x * kNqThreads + threadIdx.x; h - (threadIdx.x & 31) < nhalf;
@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kNqThreads)
     const bool act = h < nhalf;
     uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; u++) v[u] = act ? ldg_stream(w + h * 32 + u * 8) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < 4; u++)
+      v[u] = act ? __ldg(reinterpret_cast<const uint4*>(w + h * 32 + u * 8)) : make_uint4(0, 0, 0, 0);
     uint32_t m = maxabs2_nan(v[0].x, v[0].y);
     m = maxabs2_nan(m, v[0].z);
     m = maxabs2_nan(m, v[0].w);
@@ -130,8 +131,9 @@ __global__ void __launch_bounds__(kNqThreads)
 #pragma unroll
         for (int i = 0; i < 4; i++) {
           const float2 x = __fmul2_rn(widen2(wv[i]), r2);
-          c[2 * i] = nf4_code(x.x, tbl);
-          c[2 * i + 1] = nf4_code(x.y, tbl);
+          const float2 g = __ffma2_rn(x, k16, k96);
+          c[2 * i] = nf4_code(x.x, g.x, lane_tbl);
+          c[2 * i + 1] = nf4_code(x.y, g.y, lane_tbl);
         }
         // nibble j of the word is code j (a shallow tree keeps the chain short)
         const uint32_t b0 = c[0] | (c[1] << 4), b1 = c[2] | (c[3] << 4);
@@ -159,7 +161,15 @@ cudaError_t launch_nf4_quant(const uint16_t* w, int64_t n, uint8_t* codes, float
   const int64_t nhalf = n / 32;
   if (nhalf == 0) return cudaSuccess;
   const DevInfo* di = device_info();
-  const int grid = (int)std::min<int64_t>((nhalf + kNqThreads - 1) / kNqThreads, (int64_t)di->sms * 6);
+  static int per_sm = 0;  // resident CTAs per SM (registers and shared memory permitting)
+  if (per_sm == 0) {
+    cudaError_t err =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_nf4_quant, kNqThreads, kNqSmem);
+    if (err != cudaSuccess) return err;
+    per_sm = std::max(per_sm, 1);
+  }
+  const int grid =
+      (int)std::min<int64_t>((nhalf + kNqThreads - 1) / kNqThreads, (int64_t)di->sms * per_sm);
   k_nf4_quant<<<grid, kNqThreads, kNqSmem, s>>>(w, nhalf, codes, absmax, status);
   return cudaGetLastError();
 }

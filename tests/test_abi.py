@@ -51,14 +51,22 @@ def test_nf4_table_matches_oracle(nvq, oracle_mod):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-def test_nf4_bucket_design_holds_for_the_table(oracle_mod):
-    """Each 12-bit bucket (sign, exponent, 3 mantissa bits) of a normalised
-    value contains at most one midpoint of the level table -- the premise of
-    the kernel's one-comparison NF4 encoder."""
+def test_nf4_cell_design_holds_for_the_table(oracle_mod):
+    """The kernel's one-comparison NF4 encoder puts v in the cell numbered by
+    bits 17..22 of g = fl(16 v + 96); it needs every midpoint of the level
+    table in a cell of its own (g never decreases with v, so cells are
+    ordered intervals)."""
     cb = oracle_mod.nf4_codebook()
     m = ((cb[:-1] + cb[1:]) * np.float32(0.5)).astype(np.float32)
-    keys = (m.view(np.uint32) >> 20)
-    assert len(set(keys.tolist())) == 15
+    g = (m * np.float32(16.0) + np.float32(96.0)).astype(np.float32)  # 16 m exact, one rounding
+    cells = (g.view(np.uint32) >> 17) & 63
+    assert len(set(cells.tolist())) == 15
+    assert np.all(np.diff(cells.astype(np.int64)) > 0)
+    # the cell index is an ordered function of v over [-1, 1]
+    v = np.linspace(-1.0, 1.0, 200001).astype(np.float32)
+    gv = (v * np.float32(16.0) + np.float32(96.0)).astype(np.float32)
+    cv = (gv.view(np.uint32) >> 17) & 63
+    assert np.all(np.diff(cv.astype(np.int64)) >= 0)
 
 
 P = None
