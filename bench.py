@@ -361,6 +361,8 @@ def main():
     ap.add_argument("--only", default=None,
                     help="run only the calls whose name contains this text (profiling)")
     ap.add_argument("--ref-frac", type=float, default=1.0 / 8192)
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the context measurements outside the step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.experts != 256:
@@ -428,6 +430,10 @@ def main():
                      "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)} for n, ms, b in per_call}
     st = int(wl.status.item())
 
+    context = None
+    if not args.no_context:
+        context = measure_context(wl, dev, peak)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -459,6 +465,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "status_word": st,
         "clocks": sampler.summary(wall0, wall1),
+        "context": context,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
@@ -480,6 +487,72 @@ def load_traffic(kernel_name):
         return d.get(kernel_name)
     except (OSError, ValueError):
         return None
+
+
+def measure_context(wl, dev, peak):
+    """Measurements outside the step (not part of `value`): the small
+    configurations and the routing savings at small token counts.
+      * one bf16 weight [512, 256], no Four-Over-Six: quantise + dequantise,
+        launch-bound, in microseconds per pair of calls;
+      * dual-layout NVFP4 + Four-Over-Six of a 32-expert gate_up stack
+        [32, 4096, 6144] (the first 32 slices of the layer's stack);
+      * routed NF4 dequant for 8, 32 and 128 tokens of the same top-8 Zipf(1.1)
+        router: how many of the 256 experts are hit and what that costs."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    from rl_nvfp4_quantize_gb300 import synth
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+    out = {}
+    w1 = synth.single_weight(device=dev)
+    q1 = nvq.nvfp4_quantize(w1, four_over_six=False)
+    dq1 = nvq.nvfp4_dequant(q1["codes"], q1["scales"], q1["tensor_scale"])
+
+    def small():
+        nvq.nvfp4_quantize(w1, four_over_six=False, out=q1)
+        nvq.nvfp4_dequant(q1["codes"], q1["scales"], q1["tensor_scale"], out=dq1)
+    api_us = 1e3 * timed(small, 200)
+    # the same launches replayed from a CUDA graph: device time without the
+    # Python binding's per-call overhead
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        small()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        small()
+    out["single_weight_512x256_quant+dequant_us"] = {
+        "python_api": round(api_us, 2), "cuda_graph": round(1e3 * timed(graph.replay, 200), 2)}
+    E, R, K = min(32, GATE_UP[0]), GATE_UP[1], GATE_UP[2]
+    q32 = {k: v[:E] for k, v in wl.q_gu.items()}
+    n = E * R * K
+    ms = timed(lambda: nvq.nvfp4_quantize_dual(wl.gu[:E], four_over_six=True, out=q32), 5)
+    gbs = (2 * n + 2 * nvfp4_bytes(n) + 8 * E) / (ms / 1e3) / 1e9
+    out["dual_%dx%dx%d" % (E, R, K)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                        "frac": round(gbs / peak, 4)}
+    routed = {}
+    per = R * K
+    for T in (8, 32, 128):
+        topk = synth.zipf_router(T, GATE_UP[0], TOPK, seed=20 + T, device=dev)
+        ms = timed(lambda: nvq.nf4_dequant_routed(wl.nf4["codes"], wl.nf4["absmax"], topk,
+                                                  dst=wl.nf4_dst, hit_list=wl.hit, n_hit=wl.nhit), 10)
+        nh = int(wl.nhit.item())
+        b = nh * (nf4_bytes(per) + 2 * per) + T * TOPK * 4 + 4 * (GATE_UP[0] + 1)
+        routed["tokens=%d" % T] = {"experts_hit": nh, "ms": round(ms, 4),
+                                   "GB/s": round(b / (ms / 1e3) / 1e9, 1)}
+    out["nf4_dequant_routed"] = routed
+    return out
 
 
 def measure_e2e(wl, calls, steps, stream, world):
