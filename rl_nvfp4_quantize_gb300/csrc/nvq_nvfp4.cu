@@ -640,7 +640,11 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
 // phase hit eight different chunks.  One thread then stores the two boxes
 // with TMA into the [nexp, in, out] result (a 3-D map, so a ragged tile never
 // spills into the next slice).  The next tile's codes are loaded into
-// registers while the stores drain.
+// registers while the stores drain.  Each column pair of a thread's block is
+// dequantised and written to shared memory before the next, so no 8 x 8
+// output block is held in registers.  Two CTAs per SM: with a third, L1
+// shrinks to about a third and the row-strided code loads, whose 32-byte
+// sectors other warps finish using, miss it (measured 47 % slower).
 #ifndef NVQ_TQ_MINB
 #define NVQ_TQ_MINB 2
 #endif
@@ -648,13 +652,55 @@ constexpr int kTqR = 128, kTqC = 256, kTqThreads = 256;
 constexpr int kTqBox = kTqC * 64 * 2;                                  // 32 KiB per box
 constexpr int kTqSmem = 2 * kTqBox + kScaleTableBytes;                  // 64 KiB tile + table
 
+// Exact f16 pair of the two codes in byte K of w (low half = low nibble).
+template <int K>
+__device__ __forceinline__ uint32_t e2m1x2_dec_byte(uint32_t w) {
+  uint32_t h;
+  if constexpr (K == 0)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}" : "=r"(h) : "r"(w));
+  else if constexpr (K == 1)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b1;\n\t}" : "=r"(h) : "r"(w));
+  else if constexpr (K == 2)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b2;\n\t}" : "=r"(h) : "r"(w));
+  else
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b3;\n\t}" : "=r"(h) : "r"(w));
+  return h;
+}
+
+// Column pair J (block columns 2J, 2J+1) of this thread's eight out-rows:
+// dequantised and written as two 16-byte runs of the shared [in][out] tile.
+template <int J>
+__device__ __forceinline__ void dqt_column_pair(const uint2 cw[8], const uint32_t S2[8], float2 G2,
+                                                unsigned char* box, int b, int g) {
+  uint32_t v[8];  // bf16 pair (columns 2J, 2J+1) of row i
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const uint32_t h = e2m1x2_dec_byte<J & 3>(J < 4 ? cw[i].x : cw[i].y);
+    const float2 y = __fmul2_rn(cs_exact(h, S2[i]), G2);
+    v[i] = bf16x2_rn(y.x, y.y);
+  }
+  const int r = b * 16 + 2 * J;  // tile row (in-index) of column 2J
+  const int off0 = r * 128 + (((g & 7) ^ (r & 7)) << 4);
+  const int off1 = (r + 1) * 128 + (((g & 7) ^ ((r + 1) & 7)) << 4);
+  *reinterpret_cast<uint4*>(box + off0) =
+      make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                 __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410));
+  *reinterpret_cast<uint4*>(box + off1) =
+      make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632),
+                 __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632));
+}
+
 struct __align__(64) DequantTArgs {
   CUtensorMap tmap;  // dst as [nexp][in][out] bf16, boxes of 64 x 256 x 1
   const uint8_t* codes;
   const uint8_t* scales;
   const float* G;
   int out, in;
-  FastDiv per_exp, by_tiles_c;
+  FastDiv per_exp, by_tiles_r;
   uint32_t ntiles;
 };
 
@@ -669,12 +715,15 @@ __global__ void __launch_bounds__(kTqThreads, NVQ_TQ_MINB) k_dequant_t(const __g
   const int64_t in_h = in >> 1, in_16 = in >> 4;
   unsigned char* const box = tile + (g >> 3) * kTqBox;
 
+  // Consecutive tiles step along `out` first: the CTAs running at the same
+  // time then fill neighbouring 256-byte pieces of the same rows of the
+  // transposed result.
   struct Tile { uint32_t e; int r0, c0, rv, cv; };
   auto tile_of = [&](uint32_t t) {
     Tile T;
     T.e = A.per_exp.div(t);
     const uint32_t rem = t - T.e * A.per_exp.d;
-    const int tr = (int)A.by_tiles_c.div(rem), tc = (int)(rem - tr * A.by_tiles_c.d);
+    const int tc = (int)A.by_tiles_r.div(rem), tr = (int)(rem - tc * A.by_tiles_r.d);
     T.r0 = tr * kTqR;
     T.c0 = tc * kTqC;
     T.rv = min(kTqR, out - T.r0);
@@ -705,25 +754,17 @@ __global__ void __launch_bounds__(kTqThreads, NVQ_TQ_MINB) k_dequant_t(const __g
     const float Gv = A.G[T.e];
     const float2 G2 = make_float2(Gv, Gv);
     if (g * 8 < T.rv && b * 16 < T.cv) {
-      uint32_t o[8][8];  // o[i][j]: bf16 pair (columns 2j, 2j+1) of row i
+      uint32_t S2[8];
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const uint32_t S2 = pos_s2(tbl[sb[i] & 0x7f]);
-        dq_word(cw[i].x, S2, G2, o[i]);
-        dq_word(cw[i].y, S2, G2, o[i] + 4);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; j++) {
-        const int r = b * 16 + 2 * j;  // tile row (in-index) of column 2j
-        const int off0 = r * 128 + (((g & 7) ^ (r & 7)) << 4);
-        const int off1 = (r + 1) * 128 + (((g & 7) ^ ((r + 1) & 7)) << 4);
-        *reinterpret_cast<uint4*>(box + off0) =
-            make_uint4(__byte_perm(o[0][j], o[1][j], 0x5410), __byte_perm(o[2][j], o[3][j], 0x5410),
-                       __byte_perm(o[4][j], o[5][j], 0x5410), __byte_perm(o[6][j], o[7][j], 0x5410));
-        *reinterpret_cast<uint4*>(box + off1) =
-            make_uint4(__byte_perm(o[0][j], o[1][j], 0x7632), __byte_perm(o[2][j], o[3][j], 0x7632),
-                       __byte_perm(o[4][j], o[5][j], 0x7632), __byte_perm(o[6][j], o[7][j], 0x7632));
-      }
+      for (int i = 0; i < 8; i++) S2[i] = pos_s2(tbl[sb[i] & 0x7f]);
+      dqt_column_pair<0>(cw, S2, G2, box, b, g);
+      dqt_column_pair<1>(cw, S2, G2, box, b, g);
+      dqt_column_pair<2>(cw, S2, G2, box, b, g);
+      dqt_column_pair<3>(cw, S2, G2, box, b, g);
+      dqt_column_pair<4>(cw, S2, G2, box, b, g);
+      dqt_column_pair<5>(cw, S2, G2, box, b, g);
+      dqt_column_pair<6>(cw, S2, G2, box, b, g);
+      dqt_column_pair<7>(cw, S2, G2, box, b, g);
     }
     fence_proxy_async_smem();  // make this thread's tile writes visible to the TMA unit
     __syncthreads();
@@ -763,8 +804,8 @@ cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const 
   A.in = in;
   A.per_exp.d = (uint32_t)(tiles_r * tiles_c);
   make_fastdiv(A.per_exp.d, &A.per_exp.m, &A.per_exp.s);
-  A.by_tiles_c.d = (uint32_t)tiles_c;
-  make_fastdiv(A.by_tiles_c.d, &A.by_tiles_c.m, &A.by_tiles_c.s);
+  A.by_tiles_r.d = (uint32_t)tiles_r;
+  make_fastdiv(A.by_tiles_r.d, &A.by_tiles_r.m, &A.by_tiles_r.s);
   A.ntiles = (uint32_t)ntiles;
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * NVQ_TQ_MINB);
   k_dequant_t<<<grid, kTqThreads, kTqSmem, s>>>(A);
