@@ -250,6 +250,17 @@ NVQ_API int nvq_nf4_codebook(float* out);
  */
 NVQ_API int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nvq_stream_t stream);
 
+/*
+ * nvq_debug_wait_timeout -- exercises the bounded wait that every kernel of
+ * the library uses for its shared-memory copy barriers: one CTA waits, for
+ * at most `max_tries` polls, on a barrier that nothing ever completes, then
+ * ORs NVQ_STATUS_TIMEOUT into *status and returns.  No copy is in flight and
+ * nothing is left running, so the device stays usable.
+ *   max_tries  1 .. 65536 (larger values return NVQ_ERR_SHAPE)
+ *   status     device int, required
+ */
+NVQ_API int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ __all__ = [
     "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
     "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t",
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed",
-    "nf4_codebook", "debug_convert", "lib", "library_path",
+    "nf4_codebook", "debug_convert", "debug_wait_timeout", "lib", "library_path",
 ]
 
 FLAG_4OVER6 = 1
@@ -64,6 +64,7 @@ def _load():
         "nf4_dequant_routed": ([P, P, i64, i64, i64, P, i64, i64, P, P, P, P, P], i32),
         "nvq_nf4_codebook": ([P], i32),
         "nvq_debug_convert": ([i32, P, P, i64, P], i32),
+        "nvq_debug_wait_timeout": ([u32, P, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -247,3 +248,9 @@ def debug_convert(kind: int, x, stream=None):
     out = torch.empty(n * mult, dtype=dt, device=x.device)
     _check("nvq_debug_convert", lib.nvq_debug_convert(kind, _ptr(x), _ptr(out), n, _stream(stream)))
     return out
+
+
+def debug_wait_timeout(max_tries: int, status, stream=None):
+    """Runs the bounded-wait probe (see nvq_debug_wait_timeout): ORs
+    STATUS_TIMEOUT into the device int `status`."""
+    _check("nvq_debug_wait_timeout", lib.nvq_debug_wait_timeout(max_tries, _ptr(status), _stream(stream)))

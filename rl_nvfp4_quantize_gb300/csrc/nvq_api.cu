@@ -149,6 +149,23 @@ cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n,
   return cudaGetLastError();
 }
 
+// One CTA waits on a barrier that expects one arrival and never gets it.
+__global__ void k_debug_wait_timeout(uint32_t max_tries, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0, max_tries);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+}
+
+cudaError_t launch_debug_wait_timeout(uint32_t max_tries, int* status, cudaStream_t s) {
+  k_debug_wait_timeout<<<1, 32, 0, s>>>(max_tries, status);
+  return cudaGetLastError();
+}
+
 }  // namespace nvq
 
 // ---------------------------------------------------------------- the C ABI
@@ -388,6 +405,15 @@ int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nvq_stream
   int rc = device_check();
   if (rc) return rc;
   return launch_result(nvq::launch_debug_convert(kind, in, out, n, cs(stream)));
+}
+
+int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream) {
+  if (max_tries == 0 || max_tries > 65536u) return NVQ_ERR_SHAPE;
+  if (!status) return NVQ_ERR_NULL;
+  if (!aligned(status, 4)) return NVQ_ERR_ALIGN;
+  int rc = device_check();
+  if (rc) return rc;
+  return launch_result(nvq::launch_debug_wait_timeout(max_tries, status, cs(stream)));
 }
 
 }  // extern "C"

@@ -82,6 +82,7 @@ cudaError_t launch_routed_union(const int32_t* topk, int64_t n_idx, int nexp, in
                                 int32_t* n_hit, int* status, cudaStream_t s);
 
 cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n, cudaStream_t s);
+cudaError_t launch_debug_wait_timeout(uint32_t max_tries, int* status, cudaStream_t s);
 
 // The 16 NF4 levels used by the kernels (host copy).
 void nf4_levels_host(float out[16]);

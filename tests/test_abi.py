@@ -110,6 +110,10 @@ def test_validation_before_any_device_work(nvq):
     assert L.nvfp4_dequant(P, P, P, 3, 0, 16, P, P) == 0
     assert L.nf4_quantize(P, 2, 0, 64, P, P, P, P) == 0
     assert L.nvq_debug_convert(9, ok16, ok16, 4, P) == 4
+    assert L.nvq_debug_wait_timeout(0, ok16, P) == 3
+    assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3
+    assert L.nvq_debug_wait_timeout(16, P, P) == 1
+    assert L.nvq_debug_wait_timeout(16, _vp(FAKE + 2), P) == 2
 
 
 def test_valid_call_without_gpu_reports_device(nvq):
