@@ -430,14 +430,14 @@ def main():
                      "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)} for n, ms, b in per_call}
     st = int(wl.status.item())
 
-    context = None
-    if not args.no_context:
-        context = measure_context(wl, dev, peak)
-
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(wl, calls, max(2, min(args.steps, 5)), stream, world)
+
+    context = None
+    if not args.no_context:
+        context = measure_context(wl, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -447,6 +447,7 @@ def main():
                          % (desc, args.cpu_frac, sec)}
 
     traffic = load_traffic(dom[0])
+    issue = issue_view(dom[0], dom[1], GATE_UP if "gate_up" in dom[0] else DOWN)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -459,7 +460,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "traffic": traffic,
-                     "peak_source": peak_src},
+                     "peak_source": peak_src, "issue": issue},
         "hbm_frac_step": round(value / world / peak, 4),
         "breakdown": breakdown,
         "gpu_launches": launches_per_step * args.steps,
@@ -476,6 +477,29 @@ def main():
         dist.destroy_process_group()
 
 
+# Instruction issue peak of the GPU: 152 SMs x 4 schedulers x one warp
+# instruction (32 threads) per cycle at the 2070 MHz maximum SM clock.
+ISSUE_PEAK = 152 * 4 * 32 * 2.07e9
+
+
+def issue_view(kernel_name, ms, shape):
+    """The dominant call seen as instruction-issue bound: executed thread
+    instructions per second (instructions per element from the committed ncu
+    capture x elements per second measured here) against ISSUE_PEAK."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        ipe = json.load(open(p)).get("_instr_per_elem", {}).get(kernel_name)
+    except (OSError, ValueError):
+        ipe = None
+    if not ipe:
+        return None
+    n = shape[0] * shape[1] * shape[2]
+    achieved = ipe * n / (ms / 1e3)
+    return {"bound": "issue", "instr_per_elem": ipe, "achieved": round(achieved / 1e12, 2),
+            "peak": round(ISSUE_PEAK / 1e12, 2), "unit": "Tinstr/s",
+            "frac": round(achieved / ISSUE_PEAK, 4)}
+
+
 def load_traffic(kernel_name):
     """DRAM bytes per call of the dominant entry point from the committed ncu
     summary, if one was taken of the current kernels."""
@@ -484,7 +508,8 @@ def load_traffic(kernel_name):
         return None
     try:
         d = json.load(open(p))
-        return d.get(kernel_name)
+        v = d.get(kernel_name)
+        return v if isinstance(v, (int, float)) else None
     except (OSError, ValueError):
         return None
 
@@ -595,20 +620,28 @@ def measure_e2e(wl, calls, steps, stream, world):
     bi = sum(d.numel() * d.element_size() for ins, _, _ in groups for d in ins)
     bo = sum(d.numel() * d.element_size() for _, _, outs in groups for d in outs)
     step_bytes = sum(c[2] for c in calls)
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_in, s_in2, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     inputs_free = [ev() for _ in groups]    # the group's kernels no longer read its inputs
     outputs_free = [ev() for _ in groups]   # the group's results have left the device
 
     def one():
         for g, (ins, fns, outs) in enumerate(groups):
+            # each input crosses the link as two halves on two streams (one
+            # stream alone does not fill the host-to-device link)
             s_in.wait_event(inputs_free[g])
-            with torch.cuda.stream(s_in):
-                for d in ins:
-                    d.copy_(host(d), non_blocking=True)
-            arrived = ev()
-            arrived.record(s_in)
-            stream.wait_event(arrived)
+            s_in2.wait_event(inputs_free[g])
+            for d in ins:
+                flat_d, flat_h = d.view(-1), host(d).view(-1)
+                half = flat_d.numel() // 2
+                with torch.cuda.stream(s_in):
+                    flat_d[:half].copy_(flat_h[:half], non_blocking=True)
+                with torch.cuda.stream(s_in2):
+                    flat_d[half:].copy_(flat_h[half:], non_blocking=True)
+            for si in (s_in, s_in2):
+                arrived = ev()
+                arrived.record(si)
+                stream.wait_event(arrived)
             stream.wait_event(outputs_free[g])
             for fn in fns:
                 fn()
@@ -623,21 +656,21 @@ def measure_e2e(wl, calls, steps, stream, world):
     one()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     barrier(world)
     a.record(stream)
-    s_in.wait_event(a)
-    s_out.wait_event(a)
+    for si in (s_in, s_in2, s_out):
+        si.wait_event(a)
     for _ in range(steps):
         one()
-    for e, s in zip(ends, (stream, s_in, s_out)):
+    for e, s in zip(ends, (stream, s_in, s_in2, s_out)):
         e.record(s)
     torch.cuda.synchronize()
     el = max_over_ranks(world, max(a.elapsed_time(e) for e in ends) / 1e3)
     return {"value": round(job_rate(world, step_bytes, steps, el), 3), "unit": "GB/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "ms_per_step": round(1e3 * el / steps, 3),
-            "overlap": "host-to-device copies, kernels and device-to-host copies on three streams"}
+            "overlap": "host-to-device copies (two streams), kernels and device-to-host copies"}
 
 
 if __name__ == "__main__":
