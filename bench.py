@@ -226,14 +226,14 @@ def oracle_step(gu, dn, xs):
     """One pass of the oracle over a host sample (same calls as a GPU step:
     both-layout NVFP4 + Four-Over-Six with the slice amax, transposed
     dequant, per-token activations, NF4 quantise and dequant).  Returns
-    (algorithmic bytes, seconds, description)."""
+    (algorithmic bytes, seconds, description, elements)."""
     import numpy as np
     import torch
     import oracle
 
     def u16(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    total_b, secs, parts = 0, 0.0, []
+    total_b, secs, parts, elems = 0, 0.0, [], 0
     for name, w in (("gate_up", gu), ("down", dn)):
         r, K = w.shape[1], w.shape[2]
         x = u16(w)
@@ -244,6 +244,7 @@ def oracle_step(gu, dn, xs):
         secs += time.perf_counter() - t0
         n = r * K
         total_b += 2 * n + 2 * nvfp4_bytes(n) + nvfp4_bytes(n) + 2 * n
+        elems += 2 * n
         parts.append("%s[0,:%d,:]" % (name, r))
     for i, x in enumerate(xs):
         t, H = x.shape
@@ -251,6 +252,7 @@ def oracle_step(gu, dn, xs):
         oracle.act_quantize_per_token(u16(x), four_over_six=True)
         secs += time.perf_counter() - t0
         total_b += 2 * t * H + nvfp4_bytes(t * H) + 4 * t
+        elems += t * H
         parts.append("act[:%d,:%d]" % (t, H))
     r, K = gu.shape[1], gu.shape[2]
     t0 = time.perf_counter()
@@ -259,8 +261,9 @@ def oracle_step(gu, dn, xs):
     secs += time.perf_counter() - t0
     n = r * K
     total_b += 2 * n + nf4_bytes(n) + nf4_bytes(n) + 2 * n
+    elems += 2 * n
     parts.append("nf4 gate_up[0,:%d,:]" % r)
-    return total_b, secs, ", ".join(parts)
+    return total_b, secs, ", ".join(parts), elems
 
 
 def run_reference(args):
@@ -276,7 +279,7 @@ def run_reference(args):
         oracle_step(gu, dn, xs)
     tot_b, tot_s, desc = 0, 0.0, ""
     for _ in range(args.steps):
-        b, sec, desc = oracle_step(gu, dn, xs)
+        b, sec, desc, _ = oracle_step(gu, dn, xs)
         tot_b += b
         tot_s += sec
     value = tot_b / tot_s / 1e9
@@ -441,10 +444,12 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, sec, desc = oracle_step(*host_sample(args.cpu_frac, wl))
+        b, sec, desc, el = oracle_step(*host_sample(args.cpu_frac, wl))
         cpu = {"value": round(b / sec / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "%s: fraction %g of one step, %.1f s single-threaded"
-                         % (desc, args.cpu_frac, sec)}
+                         % (desc, args.cpu_frac, sec),
+               "elem_per_s": round(el / sec, 1),
+               "extrapolated_step_s": round(step_bytes / (b / sec), 1)}
 
     traffic = load_traffic(dom[0])
     issue = issue_view(dom[0], dom[1], GATE_UP if "gate_up" in dom[0] else DOWN)
