@@ -236,6 +236,30 @@ NVQ_API int nf4_dequant_routed(const uint8_t* codes, const float* absmax, int64_
 NVQ_API int nvq_nf4_codebook(float* out);
 
 /*
+ * nvfp4_dgrad -- the dgrad GEMM of routed experts read straight from their
+ * rowwise NVFP4 copy: dX = dY . DQ(Q(W_e)) for the tokens of each expert.
+ * [P4] "Key claims": the backward uses the dequantised weight
+ * x . DQ(Q(w)); [P1] "The bottom line": the rowwise copy is dequantised to
+ * bf16 for dgrad.  DQ(Q(W_e)) is the bf16 tensor nvfp4_dequant produces; it
+ * is formed in shared memory, tile by tile, and never written to HBM.  The
+ * products run on the tensor cores with FP32 accumulation, so dX matches an
+ * exact evaluation of the same sums to within FP32 rounding of the sums
+ * (|error| <= out * 2^-23 * sum |dY| |DQ|), not bit for bit.
+ *   dy           bf16 [T, out], T = sum(counts); rows of expert e follow
+ *                those of expert e-1
+ *   counts       HOST int64 [nexp]: tokens routed to each expert (>= 0)
+ *   nexp         1 .. 256
+ *   out, in      the weight slice is [out, in]; out % 64 == 0, in % 256 == 0
+ *   codes, scales, tensor_scale   the rowwise copy as nvfp4_quantize writes it
+ *   dx           FP32 [T, in], written
+ *   status       device int, nullable: NVQ_STATUS_TIMEOUT if a bounded wait
+ *                gave up (dx is then unspecified)
+ */
+NVQ_API int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int64_t out,
+                        int64_t in, const uint8_t* codes, const uint8_t* scales,
+                        const float* tensor_scale, float* dx, int* status, nvq_stream_t stream);
+
+/*
  * nvq_debug_convert -- runs one device rounding primitive elementwise, for
  * conversion sweeps against an independent implementation.
  *   kind 0: f32 -> E4M3 byte (RNE, satfinite); in f32[n], out u8[n]

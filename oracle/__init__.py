@@ -302,3 +302,40 @@ def nf4_dequant_routed(codes: np.ndarray, absmax: np.ndarray, nexp: int, rows: i
     _load().oracle_nf4_dequant_routed(_p(codes), _p(absmax), nexp, rows, cols, _p(topk), T, k,
                                       _p(dst), _p(hit), C.byref(n), C.byref(st))
     return hit, n.value, st.value
+
+
+# --- dgrad through the dequantised weight ------------------------------------
+
+def _bf16_to_f64(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact: a bf16 is the top half of an f32)."""
+    h = np.ascontiguousarray(h, np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def nvfp4_dgrad(dy: np.ndarray, counts, codes: np.ndarray, scales: np.ndarray, G: np.ndarray,
+                out: int, inn: int):
+    """dX = dY . DQ(Q(W_e)) for each expert e, in float64.
+
+    The backward of y = x . DQ(Q(w)) reads the weight through its dequantised
+    bf16 values ("The 4-bitter Lesson", "Key claims": dequantised backward;
+    "Getting GLM-5.2 NVFP4 Post-Training off the ground", "The bottom line":
+    the rowwise copy dequantised to bf16 for dgrad).  dy: bf16 bits
+    [sum(counts), out], token rows grouped by expert in expert order; codes /
+    scales / G: the rowwise NVFP4 copy of the [nexp, out, in] stack.  The
+    weight values are the oracle's own bf16 dequantisation; the contraction
+    is one float64 matrix product per expert (a library primitive).  Returns
+    (dx, bound): dx [T, in] float64 and bound = |dY| . |DQ(Q(W))|, the scale
+    of the rounding error of any float32 evaluation of the same sums."""
+    dy = np.ascontiguousarray(dy, np.uint16)
+    counts = [int(c) for c in counts]
+    dx = np.zeros((dy.shape[0], inn), np.float64)
+    bound = np.zeros_like(dx)
+    t0 = 0
+    for e, c in enumerate(counts):
+        if c:
+            w = _bf16_to_f64(nvfp4_dequant(codes[e:e + 1], scales[e:e + 1], G[e:e + 1], out, inn)[0])
+            a = _bf16_to_f64(dy[t0:t0 + c])
+            dx[t0:t0 + c] = a @ w
+            bound[t0:t0 + c] = np.abs(a) @ np.abs(w)
+        t0 += c
+    return dx, bound

@@ -23,7 +23,7 @@ import torch
 
 __all__ = [
     "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
-    "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t",
+    "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t", "nvfp4_dgrad",
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed",
     "nf4_codebook", "debug_convert", "debug_wait_timeout", "lib", "library_path",
 ]
@@ -65,6 +65,7 @@ def _load():
         "nvq_nf4_codebook": ([P], i32),
         "nvq_debug_convert": ([i32, P, P, i64, P], i32),
         "nvq_debug_wait_timeout": ([u32, P, P], i32),
+        "nvfp4_dgrad": ([P, P, i64, i64, i64, P, P, P, P, P, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -254,3 +255,21 @@ def debug_wait_timeout(max_tries: int, status, stream=None):
     """Runs the bounded-wait probe (see nvq_debug_wait_timeout): ORs
     STATUS_TIMEOUT into the device int `status`."""
     _check("nvq_debug_wait_timeout", lib.nvq_debug_wait_timeout(max_tries, _ptr(status), _stream(stream)))
+
+
+def nvfp4_dgrad(dy, counts, codes, scales, tensor_scale, status=None, stream=None, out=None):
+    """dX = dY . DQ(Q(W_e)) for the tokens routed to each expert (see
+    nvfp4_dgrad in nvq.h).  dy bf16 [T, out_dim] grouped by expert; counts:
+    tokens per expert (host sequence); codes/scales/tensor_scale: the
+    rowwise NVFP4 copy of the [nexp, out_dim, in_dim] stack.  Returns FP32
+    dX [T, in_dim]."""
+    E, R, K2 = codes.shape
+    K = K2 * 2
+    cnt = (C.c_int64 * E)(*[int(c) for c in counts])
+    T = sum(int(c) for c in counts)
+    dst = out if out is not None else _empty((T, K), torch.float32, codes)
+    _check("nvfp4_dgrad", lib.nvfp4_dgrad(_ptr(_bf16(dy, "dy")), C.cast(cnt, C.c_void_p), E, R, K,
+                                          _ptr(codes),
+                                          _ptr(scales), _ptr(tensor_scale), _ptr(dst),
+                                          _ptr(status), _stream(stream)))
+    return dst

@@ -407,6 +407,32 @@ int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nvq_stream
   return launch_result(nvq::launch_debug_convert(kind, in, out, n, cs(stream)));
 }
 
+int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int64_t out, int64_t in,
+                const uint8_t* codes, const uint8_t* scales, const float* tensor_scale, float* dx,
+                int* status, nvq_stream_t stream) {
+  if (nexp < 1 || nexp > nvq::kDgradMaxExperts || out < 0 || in < 0) return NVQ_ERR_SHAPE;
+  if (out % 64 || in % 256) return NVQ_ERR_SHAPE;
+  if (!counts) return NVQ_ERR_NULL;
+  int64_t T = 0;
+  for (int64_t e = 0; e < nexp; e++) {
+    if (counts[e] < 0) return NVQ_ERR_SHAPE;
+    T += counts[e];
+    if (T >= (1ll << 31)) return NVQ_ERR_SHAPE;
+  }
+  int64_t total;
+  if (!mul_ok(nexp, out, in, &total) || T * in >= (1ll << 40) || T * out >= (1ll << 40))
+    return NVQ_ERR_SHAPE;
+  if (T == 0 || out == 0 || in == 0) return NVQ_OK;
+  if (!dy || !codes || !scales || !tensor_scale || !dx) return NVQ_ERR_NULL;
+  if (!aligned(dy, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(dx, 16) ||
+      !aligned(tensor_scale, 4) || (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  int rc = device_check();
+  if (rc) return rc;
+  return launch_result(nvq::launch_dgrad(dy, counts, nexp, (int)out, (int)in, codes, scales,
+                                         tensor_scale, dx, status, cs(stream)));
+}
+
 int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream) {
   if (max_tries == 0 || max_tries > 65536u) return NVQ_ERR_SHAPE;
   if (!status) return NVQ_ERR_NULL;

@@ -205,6 +205,40 @@ __device__ __forceinline__ float2 resid2(uint32_t h2, uint32_t negS2, float tlo,
   return make_float2(dlo, dhi);
 }
 
+// Exact f16 pair of the two codes in byte K of w (low half = low nibble).
+template <int K>
+__device__ __forceinline__ uint32_t e2m1x2_dec_byte(uint32_t w) {
+  uint32_t h;
+  if constexpr (K == 0)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}" : "=r"(h) : "r"(w));
+  else if constexpr (K == 1)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b1;\n\t}" : "=r"(h) : "r"(w));
+  else if constexpr (K == 2)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b2;\n\t}" : "=r"(h) : "r"(w));
+  else
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b3;\n\t}" : "=r"(h) : "r"(w));
+  return h;
+}
+
+// Exact products c*S of an f16 code pair and an f16 scale pair, as FP32
+// (mixed-precision FMA c*S + (-0): the product has at most six significant
+// bits, so nothing is rounded and the sign of zero is kept).
+__device__ __forceinline__ float2 cs_exact(uint32_t h2, uint32_t S2) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 cl, ch, sl, sh;\n\t"
+      "mov.b32 {cl, ch}, %2;\n\t"
+      "mov.b32 {sl, sh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, cl, sl, 0f80000000;\n\t"
+      "fma.rn.f32.f16 %1, ch, sl, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2), "r"(S2));
+  return make_float2(lo, hi);
+}
+
 // Two FP32 -> bf16 pair (RNE); `lo` in the low half.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t d;
@@ -408,6 +442,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 // Makes barrier initialisation visible to the asynchronous (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Plain arrival (release at CTA scope): one of the barrier's expected arrivals.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {

@@ -548,21 +548,6 @@ cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* c
 // --------------------------------------------------------------- dequant
 // y = bf16( (c * S) * G ): c * S formed exactly as an f16 pair, widened to
 // FP32, multiplied by the slice's tensor scale, rounded to bf16.
-// Exact products c*S of an f16 code pair and an f16 scale pair, as FP32
-// (mixed-precision FMA c*S + (-0): the product has at most six significant
-// bits, so nothing is rounded and the sign of zero is kept).
-__device__ __forceinline__ float2 cs_exact(uint32_t h2, uint32_t S2) {
-  float lo, hi;
-  asm("{\n\t.reg .b16 cl, ch, sl, sh;\n\t"
-      "mov.b32 {cl, ch}, %2;\n\t"
-      "mov.b32 {sl, sh}, %3;\n\t"
-      "fma.rn.f32.f16 %0, cl, sl, 0f80000000;\n\t"
-      "fma.rn.f32.f16 %1, ch, sl, 0f80000000;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2), "r"(S2));
-  return make_float2(lo, hi);
-}
-
 // Dequantises the 8 codes of a word (one scale S as an f16 pair, tensor
 // scale G): four bf16 pairs, element 2j+{0,1} in word j.
 __device__ __forceinline__ void dq_word(uint32_t w, uint32_t S2, float2 G2, uint32_t o[4]) {
@@ -651,25 +636,6 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
 constexpr int kTqR = 128, kTqC = 256, kTqThreads = 256;
 constexpr int kTqBox = kTqC * 64 * 2;                                  // 32 KiB per box
 constexpr int kTqSmem = 2 * kTqBox + kScaleTableBytes;                  // 64 KiB tile + table
-
-// Exact f16 pair of the two codes in byte K of w (low half = low nibble).
-template <int K>
-__device__ __forceinline__ uint32_t e2m1x2_dec_byte(uint32_t w) {
-  uint32_t h;
-  if constexpr (K == 0)
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}" : "=r"(h) : "r"(w));
-  else if constexpr (K == 1)
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b1;\n\t}" : "=r"(h) : "r"(w));
-  else if constexpr (K == 2)
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b2;\n\t}" : "=r"(h) : "r"(w));
-  else
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b3;\n\t}" : "=r"(h) : "r"(w));
-  return h;
-}
 
 // Column pair J (block columns 2J, 2J+1) of this thread's eight out-rows:
 // dequantised and written as two 16-byte runs of the shared [in][out] tile.

@@ -110,6 +110,18 @@ def test_validation_before_any_device_work(nvq):
     assert L.nvfp4_dequant(P, P, P, 3, 0, 16, P, P) == 0
     assert L.nf4_quantize(P, 2, 0, 64, P, P, P, P) == 0
     assert L.nvq_debug_convert(9, ok16, ok16, 4, P) == 4
+    cnt = (C.c_int64 * 2)(3, 4)
+    cntp = C.cast(cnt, C.c_void_p)
+    assert L.nvfp4_dgrad(ok16, cntp, 2, 64, 200, ok16, ok16, ok16, ok16, P, P) == 3   # in % 256
+    assert L.nvfp4_dgrad(ok16, cntp, 2, 96, 256, ok16, ok16, ok16, ok16, P, P) == 3   # out % 64
+    assert L.nvfp4_dgrad(ok16, cntp, 300, 64, 256, ok16, ok16, ok16, ok16, P, P) == 3  # > 256 experts
+    assert L.nvfp4_dgrad(ok16, P, 2, 64, 256, ok16, ok16, ok16, ok16, P, P) == 1
+    assert L.nvfp4_dgrad(ok16, cntp, 2, 64, 256, ok16, ok16, ok16, P, P, P) == 1
+    assert L.nvfp4_dgrad(mis, cntp, 2, 64, 256, ok16, ok16, ok16, ok16, P, P) == 2
+    neg = (C.c_int64 * 2)(3, -1)
+    assert L.nvfp4_dgrad(ok16, C.cast(neg, C.c_void_p), 2, 64, 256, ok16, ok16, ok16, ok16, P, P) == 3
+    zero = (C.c_int64 * 2)(0, 0)
+    assert L.nvfp4_dgrad(P, C.cast(zero, C.c_void_p), 2, 64, 256, P, P, P, P, P, P) == 0
     assert L.nvq_debug_wait_timeout(0, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(16, P, P) == 1
