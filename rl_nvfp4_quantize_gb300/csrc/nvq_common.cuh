@@ -239,6 +239,15 @@ __device__ __forceinline__ float2 cs_exact(uint32_t h2, uint32_t S2) {
   return make_float2(lo, hi);
 }
 
+// E4M3 byte b -> the exact f16 pair (S, S) of its value (every E4M3 value,
+// subnormals included, is an f16).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2(uint32_t b) {
+  uint32_t h;
+  const uint16_t two = (uint16_t)(b | (b << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  return h;
+}
+
 // Two FP32 -> bf16 pair (RNE); `lo` in the low half.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t d;

@@ -8,17 +8,22 @@
 // the ground", "The bottom line" (the rowwise copy is dequantised to bf16 for
 // the dgrad GEMM instead of keeping a columnwise copy).
 //
-// Tile: 128 tokens (M) x 256 in-columns (N), K = out in steps of 64.  One CTA
-// per tile, six warps:
-//   warps 0-3 : B producers -- dequantise the 64 x 256 slice of the rowwise
+// Tile: 256 tokens (two M = 128 halves) x 256 in-columns (N), K = out in
+// steps of 64; the dequantised B slice of a K step serves both halves.  One
+// CTA per tile, ten warps:
+//   warps 0-7 : B producers -- dequantise the 64 x 256 slice of the rowwise
 //               copy (codes, scales, G) into a K-major, 128-byte-swizzled bf16
 //               tile [256 in][64 out] in shared memory; afterwards the
-//               epilogue: tensor memory -> registers -> FP32 dX rows;
-//   warp 4    : TMA loads of the dY tile [128 tokens][64 out] (same swizzle);
-//   warp 5    : allocates 256 columns of tensor memory, issues the
-//               tcgen05.mma (M 128, N 256, K 16, bf16 x bf16 -> FP32) four per
-//               K step, commits them to the stage's "empty" barrier, and frees
-//               the tensor memory at the end.
+//               epilogue (warps 0-3: tokens 0-127, warps 4-7: tokens
+//               128-255): tensor memory -> registers -> FP32 dX rows;
+//   warp 8    : TMA loads of the two dY tiles [128 tokens][64 out] (same
+//               swizzle);
+//   warp 9    : allocates all 512 columns of tensor memory (two 128 x 256
+//               FP32 accumulators), issues the tcgen05.mma (M 128, N 256,
+//               K 16, bf16 x bf16 -> FP32) -- four per K step and half, the
+//               second half only when the expert has tokens there -- commits
+//               them to the stage's "empty" barrier, and frees the tensor
+//               memory at the end.
 // Every wait is bounded; a wait that gives up sets the status word's timeout
 // bit, and every path still reaches the tensor-memory release.
 #include <cuda.h>
@@ -31,13 +36,15 @@
 namespace nvq {
 
 constexpr int kGM = 128, kGN = 256, kGK = 64;
+constexpr int kGHalves = 2;                // M halves per CTA tile
 constexpr int kGStages = 3;
-constexpr int kGA = kGM * kGK * 2;  // 16 KiB of dY per stage
-constexpr int kGB = kGN * kGK * 2;  // 32 KiB of dequantised W per stage
-constexpr int kGThreads = 192;
-constexpr int kGProducers = 128;
-constexpr uint32_t kGTmemCols = 256;  // FP32 accumulator 128 x 256
-constexpr int kGSmem = kGStages * (kGA + kGB) + kScaleTableBytes + 128;
+constexpr int kGAhead = 3;                     // K steps of codes in flight per producer
+constexpr int kGA = kGHalves * kGM * kGK * 2;  // 32 KiB of dY per stage (two 16 KiB halves)
+constexpr int kGB = kGN * kGK * 2;             // 32 KiB of dequantised W per stage
+constexpr int kGThreads = 320;
+constexpr int kGProducers = 256;
+constexpr uint32_t kGTmemCols = 512;           // two FP32 accumulators of 128 x 256
+constexpr int kGSmem = kGStages * (kGA + kGB) + 128;
 constexpr uint32_t kGWaitTries = 1u << 22;
 
 struct __align__(64) DgradArgs {
@@ -117,18 +124,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
 // B tile of one K step: out-rows k0 .. k0+63 x in-columns n0 .. n0+255 of the
 // expert's rowwise copy, written transposed ([in][out]) as 256 rows of 128
 // bytes, 16-byte chunk c of row r at chunk c ^ (r & 7).  Producer thread
-// p: out-rows 8g .. 8g+7 (g = p & 7) of 16-wide block column b = p >> 3.
+// p: out-rows 8g .. 8g+7 (g = p & 7) of 16-wide block column b = (p >> 3) & 15.
+// Producer p takes word wh = p >> 7 (columns 8 wh .. 8 wh + 7) of that block
+// column; column pair J of the word covers block columns 8 wh + 2J, +1.
 template <int J>
-__device__ __forceinline__ void dgrad_column_pair(const uint2 cw[8], const uint32_t S2[8],
-                                                  float2 G2, unsigned char* tile, int b, int g) {
+__device__ __forceinline__ void dgrad_column_pair(const uint32_t cw[8], const uint32_t S2[8],
+                                                  float2 G2, unsigned char* tile, int c0, int g) {
   uint32_t v[8];
 #pragma unroll
   for (int i = 0; i < 8; i++) {
-    const uint32_t h = e2m1x2_dec_byte<J & 3>(J < 4 ? cw[i].x : cw[i].y);
+    const uint32_t h = e2m1x2_dec_byte<J>(cw[i]);
     const float2 y = __fmul2_rn(cs_exact(h, S2[i]), G2);
     v[i] = bf16x2_rn(y.x, y.y);
   }
-  const int r = b * 16 + 2 * J;
+  const int r = c0 + 2 * J;
   *reinterpret_cast<uint4*>(tile + r * 128 + ((g ^ (r & 7)) << 4)) =
       make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
                  __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410));
@@ -141,9 +150,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_dgrad(const __grid_constant__ 
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* const sa = smem;
   unsigned char* const sb = smem + kGStages * kGA;
-  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(smem + kGStages * (kGA + kGB));
-  uint64_t* const full_a =
-      reinterpret_cast<uint64_t*>(smem + kGStages * (kGA + kGB) + kScaleTableBytes);
+  uint64_t* const full_a = reinterpret_cast<uint64_t*>(smem + kGStages * (kGA + kGB));
   uint64_t* const full_b = full_a + kGStages;
   uint64_t* const empty = full_b + kGStages;
   uint64_t* const acc_bar = empty + kGStages;
@@ -166,70 +173,77 @@ __global__ void __launch_bounds__(kGThreads, 1) k_dgrad(const __grid_constant__ 
   const int e = lo;
   const int local = tile - A.tile_off[e];
   const int mt = local / A.tiles_n, nt = local - mt * A.tiles_n;
-  const int tok0 = A.tok_off[e] + mt * kGM, tok_end = A.tok_off[e + 1];
+  const int tok0 = A.tok_off[e] + mt * (kGHalves * kGM), tok_end = A.tok_off[e + 1];
+  const bool two = tok0 + kGM < tok_end;  // the second half has tokens of this expert
   const int n0 = nt * kGN;
   const int nk = A.out / kGK;
 
-  build_scale_table(tbl);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGStages; s++) {
       mbar_init(&full_a[s], 1);
-      mbar_init(&full_b[s], kGProducers);
+      mbar_init(&full_b[s], kGProducers / 32);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_bar, 1);
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, kGTmemCols);
+  if (warp == 9) tmem_alloc(tmem_slot, kGTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   bool ok = true;
-  if (warp < 4) {
+  if (warp < 8) {
     // ---- B producers
-    const int p = threadIdx.x, g = p & 7, b = p >> 3;
+    const int p = threadIdx.x, g = p & 7, b = (p >> 3) & 15, wh = p >> 7;
     const int64_t in_h = A.in >> 1, in_16 = A.in >> 4;
-    const uint8_t* pc0 = A.codes + (int64_t)e * A.out * in_h + (n0 >> 1) + b * 8;
+    const uint8_t* pc0 = A.codes + (int64_t)e * A.out * in_h + (n0 >> 1) + b * 8 + wh * 4;
     const uint8_t* ps0 = A.scales + (int64_t)e * A.out * in_16 + (n0 >> 4) + b;
     const float Gv = A.G[e];
     const float2 G2 = make_float2(Gv, Gv);
-    uint2 cw[8];
-    uint32_t sbyte[8];
-    auto load = [&](int ks) {
+    const int c0 = b * 16 + wh * 8;  // first tile row (in-index) of this thread
+    // codes and scale bytes of K step ks, loaded kGAhead steps before use
+    // into one of kGAhead register buffers (the loop is unrolled by kGAhead
+    // so every buffer index is a constant)
+    uint32_t cw[kGAhead][8], sbyte[kGAhead][8];
+    auto load = [&](int ks, uint32_t* c, uint32_t* sbv) {
       const int64_t row = (int64_t)ks * kGK + g * 8;
 #pragma unroll
       for (int i = 0; i < 8; i++) {
-        cw[i] = __ldg(reinterpret_cast<const uint2*>(pc0 + (row + i) * in_h));
-        sbyte[i] = __ldg(ps0 + (row + i) * in_16);
+        c[i] = __ldg(reinterpret_cast<const uint32_t*>(pc0 + (row + i) * in_h));
+        sbv[i] = __ldg(ps0 + (row + i) * in_16);
       }
     };
-    load(0);
-    for (int ks = 0; ks < nk; ks++) {
-      const int s = ks % kGStages, u = ks / kGStages;
-      if (ks >= kGStages && !mbar_wait(&empty[s], (u - 1) & 1, kGWaitTries)) {
-        ok = false;
-        break;
-      }
-      uint32_t S2[8];
 #pragma unroll
-      for (int i = 0; i < 8; i++) S2[i] = pos_s2(tbl[sbyte[i] & 0x7f]);
-      const uint2 cur[8] = {cw[0], cw[1], cw[2], cw[3], cw[4], cw[5], cw[6], cw[7]};
-      if (ks + 1 < nk) load(ks + 1);
+    for (int j = 0; j < kGAhead; j++)
+      if (j < nk) load(j, cw[j], sbyte[j]);
+    auto step = [&](int ks, uint32_t* c, uint32_t* sbv) -> bool {
+      const int s = ks % kGStages, u = ks / kGStages;
+      if (ks >= kGStages && !mbar_wait(&empty[s], (u - 1) & 1, kGWaitTries)) return false;
+      uint32_t S2[8], cur[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        S2[i] = e4m3_to_f16x2(sbv[i] & 0x7f);
+        cur[i] = c[i];
+      }
+      if (ks + kGAhead < nk) load(ks + kGAhead, c, sbv);
       unsigned char* tileb = sb + s * kGB;
-      dgrad_column_pair<0>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<1>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<2>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<3>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<4>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<5>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<6>(cur, S2, G2, tileb, b, g);
-      dgrad_column_pair<7>(cur, S2, G2, tileb, b, g);
+      dgrad_column_pair<0>(cur, S2, G2, tileb, c0, g);
+      dgrad_column_pair<1>(cur, S2, G2, tileb, c0, g);
+      dgrad_column_pair<2>(cur, S2, G2, tileb, c0, g);
+      dgrad_column_pair<3>(cur, S2, G2, tileb, c0, g);
       fence_proxy_async_smem();  // the tensor cores read the tile through the async proxy
-      mbar_arrive(&full_b[s]);
+      __syncwarp();              // then one arrival per warp
+      if (lane == 0) mbar_arrive(&full_b[s]);
+      return true;
+    };
+    for (int k0 = 0; k0 < nk && ok; k0 += kGAhead) {
+#pragma unroll
+      for (int j = 0; j < kGAhead; j++)
+        if (ok && k0 + j < nk) ok = step(k0 + j, cw[j], sbyte[j]);
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ---- dY tiles by TMA
     if (lane == 0) {
       int issued = 0;
@@ -241,6 +255,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_dgrad(const __grid_constant__ 
         }
         mbar_arrive_expect_tx(&full_a[s], kGA);
         tma_load_2d(sa + s * kGA, &A.tmap_a, ks * kGK, tok0, &full_a[s]);
+        tma_load_2d(sa + s * kGA + kGA / 2, &A.tmap_a, ks * kGK, tok0 + kGM, &full_a[s]);
         issued = ks + 1;
       }
       if (!ok) {  // let the copies already issued land before the CTA leaves
@@ -248,7 +263,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_dgrad(const __grid_constant__ 
           mbar_wait(&full_a[ks % kGStages], (ks / kGStages) & 1, kGWaitTries);
       }
     }
-  } else {
+  } else if (warp == 9) {
     // ---- tensor-core issue
     if (lane == 0) {
       for (int ks = 0; ks < nk; ks++) {
@@ -261,30 +276,34 @@ __global__ void __launch_bounds__(kGThreads, 1) k_dgrad(const __grid_constant__ 
         tc_fence_after();
         const uint32_t a0 = smem_u32(sa + s * kGA), b0 = smem_u32(sb + s * kGB);
 #pragma unroll
-        for (int kk = 0; kk < kGK / 16; kk++)
-          umma_bf16(tmem, umma_desc_k_sw128(a0 + kk * 32), umma_desc_k_sw128(b0 + kk * 32),
-                    (ks | kk) != 0);
+        for (int kk = 0; kk < kGK / 16; kk++) {
+          const uint64_t bd = umma_desc_k_sw128(b0 + kk * 32);
+          umma_bf16(tmem, umma_desc_k_sw128(a0 + kk * 32), bd, (ks | kk) != 0);
+          if (two)
+            umma_bf16(tmem + kGN, umma_desc_k_sw128(a0 + kGA / 2 + kk * 32), bd, (ks | kk) != 0);
+        }
         umma_commit(&empty[s]);
       }
       umma_commit(acc_bar);  // also after a failed wait: covers what was issued
     }
   }
 
-  // ---- epilogue: warps 0-3 read lanes 32w .. 32w+31 of the accumulator
+  // ---- epilogue: warp w reads lanes 32 (w & 3) .. +31 of accumulator w >> 2
   __syncwarp();
-  if (warp < 4) {
+  if (warp < 8) {
+    const int half = warp >> 2, q = warp & 3;
     // tcgen05.ld is executed by whole warps, so the warp agrees on the wait
     if (!__all_sync(0xffffffffu, mbar_wait(acc_bar, 0, kGWaitTries))) {
       ok = false;
-    } else {
+    } else if (half == 0 || two) {
       tc_fence_after();
-      const int row = tok0 + warp * 32 + lane;
+      const int row = tok0 + half * kGM + q * 32 + lane;
       float* dst = A.dx + (int64_t)row * A.in + n0;
       const bool store = ok && row < tok_end;
 #pragma unroll 1
       for (int c = 0; c < kGN / 32; c++) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, v);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * kGN + c * 32, v);
         if (store) {
 #pragma unroll
           for (int j = 0; j < 8; j++)
@@ -293,14 +312,14 @@ __global__ void __launch_bounds__(kGThreads, 1) k_dgrad(const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 5 && lane == 0) {
+  } else if (warp == 9 && lane == 0) {
     // the tensor memory is released only after every issued MMA has finished
     if (!mbar_wait(acc_bar, 0, kGWaitTries)) ok = false;
   }
   if (!ok && A.status) atomicOr(A.status, kStatusTimeout);
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kGTmemCols);
@@ -324,7 +343,7 @@ cudaError_t launch_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp
     A.tok_off[e] = (int)tok;
     A.tile_off[e] = (int)tiles;
     tok += counts[e];
-    tiles += (counts[e] + kGM - 1) / kGM * tiles_n;
+    tiles += (counts[e] + kGHalves * kGM - 1) / (kGHalves * kGM) * tiles_n;
   }
   A.tok_off[nexp] = (int)tok;
   A.tile_off[nexp] = (int)tiles;
