@@ -582,7 +582,53 @@ def measure_context(wl, dev, peak):
         routed["tokens=%d" % T] = {"experts_hit": nh, "ms": round(ms, 4),
                                    "GB/s": round(b / (ms / 1e3) / 1e9, 1)}
     out["nf4_dequant_routed"] = routed
+    out["nvfp4_dgrad"] = measure_dgrad(wl, dev, timed)
     return out
+
+
+def measure_dgrad(wl, dev, timed):
+    """The dgrad GEMM of the layer's routed experts read straight from the
+    rowwise NVFP4 copies (tensor cores, dequantisation fused into the B
+    operand): dX = dY . DQ(Q(W_e)) for the tokens the router sends to each
+    expert, for gate_up and down, against the measured dense bf16 peak; and
+    the same product as a dequantisation to bf16 followed by one cuBLAS
+    matmul per expert, for comparison."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    from rl_nvfp4_quantize_gb300 import synth
+    peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        peak = float(json.load(open(p)).get("bf16_tflops", 0)) or None
+    counts = torch.bincount(wl.topk.flatten().long(), minlength=GATE_UP[0]).cpu().tolist()
+    T = sum(counts)
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    res = {}
+    for name, q, (E, R, K) in (("gate_up", wl.q_gu, GATE_UP), ("down", wl.q_dn, DOWN)):
+        dy = synth.activations(T, R, seed=41, device=dev)
+        dx = torch.empty((T, K), dtype=torch.float32, device=dev)
+        ms = timed(lambda: nvq.nvfp4_dgrad(dy, counts, q["codes_row"], q["scales_row"],
+                                           q["tensor_scale"], out=dx), 5)
+        flops = 2.0 * T * R * K
+        wd = torch.empty((E, R, K), dtype=torch.bfloat16, device=dev)
+        dxb = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+
+        def unfused():
+            nvq.nvfp4_dequant(q["codes_row"], q["scales_row"], q["tensor_scale"], out=wd)
+            for e in range(E):
+                if counts[e]:
+                    torch.matmul(dy[offs[e]:offs[e + 1]], wd[e], out=dxb[offs[e]:offs[e + 1]])
+        ms_u = timed(unfused, 3)
+        tf = flops / (ms / 1e3) / 1e12
+        res[name] = {"tokens": T, "ms": round(ms, 3), "TFLOP/s": round(tf, 1),
+                     "bound": "tensor", "peak_bf16_TFLOP/s": peak,
+                     "frac": round(tf / peak, 4) if peak else None,
+                     "dequant_then_cublas_ms": round(ms_u, 3)}
+        del dy, dx, wd, dxb
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_e2e(wl, calls, steps, stream, world):
