@@ -366,10 +366,21 @@ def main():
     ap.add_argument("--ref-frac", type=float, default=1.0 / 8192)
     ap.add_argument("--no-context", action="store_true",
                     help="skip the context measurements outside the step")
+    ap.add_argument("--unfused", action="store_true",
+                    help="with --case: also time the dequant + per-expert cuBLAS comparison")
+    ap.add_argument("--case", default=None, choices=["dgrad", "nf4_linear"],
+                    help="run one context measurement alone on a reduced case (profiling)")
+    ap.add_argument("--tokens", type=int, default=2048,
+                    help="router tokens of --case")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.experts != 256:
         set_experts(args.experts)
+    if args.case:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_case(args)
+        return
 
     import __graft_entry__
     __graft_entry__.build()
@@ -519,6 +530,22 @@ def load_traffic(kernel_name):
         return None
 
 
+def cuda_timed(fn, reps):
+    """Mean device time of one call in ms: three warm-up calls, then `reps`
+    calls between two CUDA events on the current stream."""
+    import torch
+    for _ in range(3):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
 def measure_context(wl, dev, peak):
     """Measurements outside the step (not part of `value`): the small
     configurations and the routing savings at small token counts.
@@ -532,17 +559,7 @@ def measure_context(wl, dev, peak):
     import rl_nvfp4_quantize_gb300 as nvq
     from rl_nvfp4_quantize_gb300 import synth
 
-    def timed(fn, reps):
-        for _ in range(3):
-            fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record()
-        for _ in range(reps):
-            fn()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+    timed = cuda_timed
     out = {}
     w1 = synth.single_weight(device=dev)
     q1 = nvq.nvfp4_quantize(w1, four_over_six=False)
@@ -582,11 +599,15 @@ def measure_context(wl, dev, peak):
         routed["tokens=%d" % T] = {"experts_hit": nh, "ms": round(ms, 4),
                                    "GB/s": round(b / (ms / 1e3) / 1e9, 1)}
     out["nf4_dequant_routed"] = routed
-    out["nvfp4_dgrad"] = measure_dgrad(wl, dev, timed)
+    stacks = {"gate_up": (wl.q_gu["codes_row"], wl.q_gu["scales_row"], wl.q_gu["tensor_scale"], GATE_UP),
+              "down": (wl.q_dn["codes_row"], wl.q_dn["scales_row"], wl.q_dn["tensor_scale"], DOWN)}
+    out["nvfp4_dgrad"] = measure_dgrad(stacks, wl.topk, dev)
+    out["nf4_routed_linear"] = measure_nf4_linear(
+        {"gate_up": (wl.nf4["codes"], wl.nf4["absmax"], GATE_UP)}, wl.topk, dev)
     return out
 
 
-def measure_dgrad(wl, dev, timed):
+def measure_dgrad(stacks, topk, dev, unfused=True):
     """The dgrad GEMM of the layer's routed experts read straight from the
     rowwise NVFP4 copies (tensor cores, dequantisation fused into the B
     operand): dX = dY . DQ(Q(W_e)) for the tokens the router sends to each
@@ -600,35 +621,116 @@ def measure_dgrad(wl, dev, timed):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         peak = float(json.load(open(p)).get("bf16_tflops", 0)) or None
-    counts = torch.bincount(wl.topk.flatten().long(), minlength=GATE_UP[0]).cpu().tolist()
+    nexp = next(iter(stacks.values()))[3][0]
+    counts = torch.bincount(topk.flatten().long(), minlength=nexp).cpu().tolist()
     T = sum(counts)
     offs = [0]
     for c in counts:
         offs.append(offs[-1] + c)
     res = {}
-    for name, q, (E, R, K) in (("gate_up", wl.q_gu, GATE_UP), ("down", wl.q_dn, DOWN)):
+    for name, (codes, scales, G, (E, R, K)) in stacks.items():
         dy = synth.activations(T, R, seed=41, device=dev)
         dx = torch.empty((T, K), dtype=torch.float32, device=dev)
-        ms = timed(lambda: nvq.nvfp4_dgrad(dy, counts, q["codes_row"], q["scales_row"],
-                                           q["tensor_scale"], out=dx), 5)
+        ms = cuda_timed(lambda: nvq.nvfp4_dgrad(dy, counts, codes, scales, G, out=dx), 5)
         flops = 2.0 * T * R * K
-        wd = torch.empty((E, R, K), dtype=torch.bfloat16, device=dev)
-        dxb = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
-
-        def unfused():
-            nvq.nvfp4_dequant(q["codes_row"], q["scales_row"], q["tensor_scale"], out=wd)
-            for e in range(E):
-                if counts[e]:
-                    torch.matmul(dy[offs[e]:offs[e + 1]], wd[e], out=dxb[offs[e]:offs[e + 1]])
-        ms_u = timed(unfused, 3)
         tf = flops / (ms / 1e3) / 1e12
         res[name] = {"tokens": T, "ms": round(ms, 3), "TFLOP/s": round(tf, 1),
                      "bound": "tensor", "peak_bf16_TFLOP/s": peak,
-                     "frac": round(tf / peak, 4) if peak else None,
-                     "dequant_then_cublas_ms": round(ms_u, 3)}
-        del dy, dx, wd, dxb
+                     "frac": round(tf / peak, 4) if peak else None}
+        del dx
+        if unfused:
+            wd = torch.empty((E, R, K), dtype=torch.bfloat16, device=dev)
+            dxb = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+
+            def dequant_then_matmul():
+                nvq.nvfp4_dequant(codes, scales, G, out=wd)
+                for e in range(E):
+                    if counts[e]:
+                        torch.matmul(dy[offs[e]:offs[e + 1]], wd[e], out=dxb[offs[e]:offs[e + 1]])
+            res[name]["dequant_then_cublas_ms"] = round(cuda_timed(dequant_then_matmul, 3), 3)
+            del wd, dxb
+        del dy
         torch.cuda.empty_cache()
     return res
+
+
+def measure_nf4_linear(stacks, topk, dev, unfused=True):
+    """The forward product of the routed experts read straight from their NF4
+    copies (tensor cores, dequantisation fused into the B operand):
+    Y = X . DQ(W_e)^T for the tokens the router sends to each expert, against
+    the measured dense bf16 peak; and the same product as the routed dequant
+    to bf16 followed by one cuBLAS matmul per expert, for comparison."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    from rl_nvfp4_quantize_gb300 import synth
+    peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        peak = float(json.load(open(p)).get("bf16_tflops", 0)) or None
+    nexp = next(iter(stacks.values()))[2][0]
+    counts = torch.bincount(topk.flatten().long(), minlength=nexp).cpu().tolist()
+    T = sum(counts)
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    res = {}
+    for name, (codes, absmax, (E, R, K)) in stacks.items():
+        x = synth.activations(T, K, seed=43, device=dev)
+        y = torch.empty((T, R), dtype=torch.bfloat16, device=dev)
+        ms = cuda_timed(lambda: nvq.nf4_routed_linear(x, counts, codes, absmax, out=y), 5)
+        flops = 2.0 * T * R * K
+        tf = flops / (ms / 1e3) / 1e12
+        res[name] = {"tokens": T, "ms": round(ms, 3), "TFLOP/s": round(tf, 1),
+                     "bound": "tensor", "peak_bf16_TFLOP/s": peak,
+                     "frac": round(tf / peak, 4) if peak else None}
+        if unfused:
+            wd = torch.empty((E, R, K), dtype=torch.bfloat16, device=dev)
+            hit = torch.empty((E,), dtype=torch.int32, device=dev)
+            nh = torch.empty((1,), dtype=torch.int32, device=dev)
+
+            def dequant_then_matmul():
+                nvq.nf4_dequant_routed(codes, absmax, topk, dst=wd, hit_list=hit, n_hit=nh)
+                for e in range(E):
+                    if counts[e]:
+                        torch.matmul(x[offs[e]:offs[e + 1]], wd[e].t(), out=y[offs[e]:offs[e + 1]])
+            res[name]["dequant_then_cublas_ms"] = round(cuda_timed(dequant_then_matmul, 3), 3)
+            del wd
+        del x, y
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_case(args):
+    """One context measurement alone, on a reduced expert count and router
+    (the small cases the ncu captures use): --case dgrad quantises gate_up
+    and down stacks of --experts slices rowwise (NVFP4, Four-Over-Six),
+    --case nf4_linear quantises them to NF4; both route --tokens tokens top-8
+    with the Zipf(1.1) router and time nvfp4_dgrad / nf4_routed_linear on
+    both stacks (the cuBLAS comparison only with --unfused).  Prints one JSON
+    object."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    from rl_nvfp4_quantize_gb300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    E = GATE_UP[0]
+    stacks = {}
+    for name, shape, seed in (("gate_up", GATE_UP, 2), ("down", DOWN, 3)):
+        w = synth.expert_weights(*shape, seed=seed, device=dev)
+        if args.case == "dgrad":
+            q = nvq.nvfp4_quantize(w, four_over_six=True)
+            stacks[name] = (q["codes"], q["scales"], q["tensor_scale"], shape)
+        else:
+            q = nvq.nf4_quantize(w)
+            stacks[name] = (q["codes"], q["absmax"], shape)
+        del w
+    topk = synth.zipf_router(args.tokens, E, TOPK, seed=6, device=dev)
+    if args.case == "dgrad":
+        res = measure_dgrad(stacks, topk, dev, unfused=args.unfused)
+    else:
+        res = measure_nf4_linear(stacks, topk, dev, unfused=args.unfused)
+    print(json.dumps({"case": args.case, "experts": E, "tokens": args.tokens, "topk": TOPK,
+                      "result": res}))
 
 
 def measure_e2e(wl, calls, steps, stream, world):

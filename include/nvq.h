@@ -251,13 +251,39 @@ NVQ_API int nvq_nf4_codebook(float* out);
  *   nexp         1 .. 256
  *   out, in      the weight slice is [out, in]; out % 64 == 0, in % 256 == 0
  *   codes, scales, tensor_scale   the rowwise copy as nvfp4_quantize writes it
- *   dx           FP32 [T, in], written
+ *   dx           FP32 [T, in], written (zeros when out == 0)
  *   status       device int, nullable: NVQ_STATUS_TIMEOUT if a bounded wait
  *                gave up (dx is then unspecified)
  */
 NVQ_API int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int64_t out,
                         int64_t in, const uint8_t* codes, const uint8_t* scales,
                         const float* tensor_scale, float* dx, int* status, nvq_stream_t stream);
+
+/*
+ * nf4_routed_linear -- the forward product of routed experts stored as NF4:
+ * Y = X . DQ(W_e)^T for the tokens routed to each expert e.  [P5] "The fix:
+ * dequant-on-forward for routed experts": each routed expert's weight is
+ * dequantised to bf16 and applied as F.linear(x, W[e]) to the tokens sent to
+ * it; "Making it fast: the step tax": the dequantised copies are the per-step
+ * cost.  DQ(W_e) is the bf16 tensor nf4_dequant produces; it is formed in
+ * shared memory, tile by tile, and never written to HBM.  The products run on
+ * the tensor cores with FP32 accumulation and Y is the bf16 round to nearest
+ * even of the FP32 sum, so |Y - exact| <= 2^-8 (|exact| + d) + d with
+ * d = in * 2^-23 * sum |X| |DQ| (not bit for bit).
+ *   x            bf16 [T, in], T = sum(counts); rows of expert e follow those
+ *                of expert e-1 (the caller sorts tokens by expert)
+ *   counts       HOST int64 [nexp]: tokens routed to each expert (>= 0)
+ *   nexp         1 .. 256
+ *   out, in      the weight slice is [out, in]; out % 256 == 0, in % 64 == 0
+ *   codes        u8 [nexp, out, in/2] as nf4_quantize writes them (32-byte
+ *                aligned); absmax f32 [nexp, out, in/64]
+ *   y            bf16 [T, out], written (zeros when in == 0)
+ *   status       device int, nullable: NVQ_STATUS_TIMEOUT if a bounded wait
+ *                gave up (y is then unspecified)
+ */
+NVQ_API int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, int64_t out,
+                              int64_t in, const uint8_t* codes, const float* absmax, uint16_t* y,
+                              int* status, nvq_stream_t stream);
 
 /*
  * nvq_debug_convert -- runs one device rounding primitive elementwise, for

@@ -339,3 +339,33 @@ def nvfp4_dgrad(dy: np.ndarray, counts, codes: np.ndarray, scales: np.ndarray, G
             bound[t0:t0 + c] = np.abs(a) @ np.abs(w)
         t0 += c
     return dx, bound
+
+
+def nf4_routed_linear(x: np.ndarray, counts, codes: np.ndarray, absmax: np.ndarray, out: int,
+                      inn: int):
+    """Y = X . DQ(W_e)^T for each expert e, in float64.
+
+    The forward of a routed expert stored as NF4 dequantises its weight to
+    bf16 and applies it to the tokens sent to it ("nf4moe -- QLoRA for a 743B
+    Fused-MoE", "The fix: dequant-on-forward for routed experts": F.linear(x,
+    W[e]) on the dequantised W[e]).  x: bf16 bits [sum(counts), in], token
+    rows grouped by expert in expert order; codes / absmax: the NF4 copy of
+    the [nexp, out, in] stack.  The weight values are the oracle's own bf16
+    dequantisation; the contraction is one float64 matrix product per expert
+    (a library primitive).  Returns (y, bound): y [T, out] float64, exact up
+    to float64 rounding, and bound = |X| . |DQ(W)|^T, the scale of the
+    rounding error of any float32 evaluation of the same sums."""
+    x = np.ascontiguousarray(x, np.uint16)
+    counts = [int(c) for c in counts]
+    y = np.zeros((x.shape[0], out), np.float64)
+    bound = np.zeros_like(y)
+    t0 = 0
+    for e, c in enumerate(counts):
+        if c:
+            w = _bf16_to_f64(nf4_dequant(codes[e:e + 1], absmax[e:e + 1], 1, out, inn)[0])
+            a = _bf16_to_f64(x[t0:t0 + c])
+            y[t0:t0 + c] = a @ w.T
+            bound[t0:t0 + c] = np.abs(a) @ np.abs(w).T
+        t0 += c
+    return y, bound
+

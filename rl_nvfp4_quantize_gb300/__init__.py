@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
     "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t", "nvfp4_dgrad",
-    "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed",
+    "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed", "nf4_routed_linear",
     "nf4_codebook", "debug_convert", "debug_wait_timeout", "lib", "library_path",
 ]
 
@@ -66,6 +66,7 @@ def _load():
         "nvq_debug_convert": ([i32, P, P, i64, P], i32),
         "nvq_debug_wait_timeout": ([u32, P, P], i32),
         "nvfp4_dgrad": ([P, P, i64, i64, i64, P, P, P, P, P, P], i32),
+        "nf4_routed_linear": ([P, P, i64, i64, i64, P, P, P, P, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -272,4 +273,20 @@ def nvfp4_dgrad(dy, counts, codes, scales, tensor_scale, status=None, stream=Non
                                           _ptr(codes),
                                           _ptr(scales), _ptr(tensor_scale), _ptr(dst),
                                           _ptr(status), _stream(stream)))
+    return dst
+
+
+def nf4_routed_linear(x, counts, codes, absmax, status=None, stream=None, out=None):
+    """Y = X . DQ(W_e)^T for the tokens routed to each expert (see
+    nf4_routed_linear in nvq.h).  x bf16 [T, in_dim] grouped by expert;
+    counts: tokens per expert (host sequence); codes/absmax: the NF4 copy of
+    the [nexp, out_dim, in_dim] stack.  Returns bf16 Y [T, out_dim]."""
+    E, R, K2 = codes.shape
+    K = K2 * 2
+    cnt = (C.c_int64 * E)(*[int(c) for c in counts])
+    T = sum(int(c) for c in counts)
+    dst = out if out is not None else _empty((T, R), torch.bfloat16, codes)
+    _check("nf4_routed_linear", lib.nf4_routed_linear(_ptr(_bf16(x, "x")), C.cast(cnt, C.c_void_p),
+                                                      E, R, K, _ptr(codes), _ptr(absmax), _ptr(dst),
+                                                      _ptr(status), _stream(stream)))
     return dst

@@ -410,7 +410,7 @@ int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nvq_stream
 int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int64_t out, int64_t in,
                 const uint8_t* codes, const uint8_t* scales, const float* tensor_scale, float* dx,
                 int* status, nvq_stream_t stream) {
-  if (nexp < 1 || nexp > nvq::kDgradMaxExperts || out < 0 || in < 0) return NVQ_ERR_SHAPE;
+  if (nexp < 1 || nexp > nvq::kGroupedMaxExperts || out < 0 || in < 0) return NVQ_ERR_SHAPE;
   if (out % 64 || in % 256) return NVQ_ERR_SHAPE;
   if (!counts) return NVQ_ERR_NULL;
   int64_t T = 0;
@@ -422,15 +422,48 @@ int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int64_t
   int64_t total;
   if (!mul_ok(nexp, out, in, &total) || T * in >= (1ll << 40) || T * out >= (1ll << 40))
     return NVQ_ERR_SHAPE;
-  if (T == 0 || out == 0 || in == 0) return NVQ_OK;
-  if (!dy || !codes || !scales || !tensor_scale || !dx) return NVQ_ERR_NULL;
-  if (!aligned(dy, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(dx, 16) ||
-      !aligned(tensor_scale, 4) || (status && !aligned(status, 4)))
+  if (T == 0 || in == 0) return NVQ_OK;
+  const bool contract = out > 0;  // out == 0: an empty contraction, dX = 0
+  if (!dx || (contract && (!dy || !codes || !scales || !tensor_scale))) return NVQ_ERR_NULL;
+  if (!aligned(dx, 16) || (status && !aligned(status, 4)) ||
+      (contract && (!aligned(dy, 16) || !aligned(codes, 16) || !aligned(scales, 16) ||
+                    !aligned(tensor_scale, 4))))
     return NVQ_ERR_ALIGN;
   int rc = device_check();
   if (rc) return rc;
+  if (!contract)
+    return launch_result(cudaMemsetAsync(dx, 0, (size_t)(T * in) * sizeof(float), cs(stream)));
   return launch_result(nvq::launch_dgrad(dy, counts, nexp, (int)out, (int)in, codes, scales,
                                          tensor_scale, dx, status, cs(stream)));
+}
+
+int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, int64_t out,
+                      int64_t in, const uint8_t* codes, const float* absmax, uint16_t* y,
+                      int* status, nvq_stream_t stream) {
+  if (nexp < 1 || nexp > nvq::kGroupedMaxExperts || out < 0 || in < 0) return NVQ_ERR_SHAPE;
+  if (out % 256 || in % 64) return NVQ_ERR_SHAPE;
+  if (!counts) return NVQ_ERR_NULL;
+  int64_t T = 0;
+  for (int64_t e = 0; e < nexp; e++) {
+    if (counts[e] < 0) return NVQ_ERR_SHAPE;
+    T += counts[e];
+    if (T >= (1ll << 31)) return NVQ_ERR_SHAPE;
+  }
+  int64_t total;
+  if (!mul_ok(nexp, out, in, &total) || T * in >= (1ll << 40) || T * out >= (1ll << 40))
+    return NVQ_ERR_SHAPE;
+  if (T == 0 || out == 0) return NVQ_OK;
+  const bool contract = in > 0;  // in == 0: an empty contraction, Y = 0
+  if (!y || (contract && (!x || !codes || !absmax))) return NVQ_ERR_NULL;
+  if (!aligned(y, 16) || (status && !aligned(status, 4)) ||
+      (contract && (!aligned(x, 16) || !aligned(codes, 32) || !aligned(absmax, 16))))
+    return NVQ_ERR_ALIGN;
+  int rc = device_check();
+  if (rc) return rc;
+  if (!contract)
+    return launch_result(cudaMemsetAsync(y, 0, (size_t)(T * out) * sizeof(uint16_t), cs(stream)));
+  return launch_result(nvq::launch_nf4_linear(x, counts, nexp, (int)out, (int)in, codes, absmax,
+                                              y, status, cs(stream)));
 }
 
 int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream) {

@@ -83,12 +83,15 @@ cudaError_t launch_routed_union(const int32_t* topk, int64_t n_idx, int nexp, in
 
 cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n, cudaStream_t s);
 cudaError_t launch_debug_wait_timeout(uint32_t max_tries, int* status, cudaStream_t s);
-// Experts per nvfp4_dgrad call (their token and tile offsets travel in the
-// kernel's parameter block).
-constexpr int kDgradMaxExperts = 256;
+// Experts per grouped-GEMM call (nvfp4_dgrad, nf4_routed_linear): their
+// token and tile offsets travel in the kernel's parameter block.
+constexpr int kGroupedMaxExperts = 256;
 cudaError_t launch_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int out, int in,
                          const uint8_t* codes, const uint8_t* scales, const float* G, float* dx,
                          int* status, cudaStream_t s);
+cudaError_t launch_nf4_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, int out,
+                              int in, const uint8_t* codes, const float* absmax, uint16_t* y,
+                              int* status, cudaStream_t s);
 
 // The 16 NF4 levels used by the kernels (host copy).
 void nf4_levels_host(float out[16]);

@@ -6,7 +6,8 @@ The tensor cores accumulate in FP32 in an order of their own, so the check is
 at most `out` products, each addition rounded once (with 2^-23 instead of
 2^-24 for the rounding unit, to allow for truncation).  A separate case uses a
 weight whose dequantised values and an integer dY make every sum exact, where
-the result must match bit for bit.
+the result must match bit for bit.  Both sides read the rowwise NVFP4 copy
+the oracle makes of the weight.
 """
 import numpy as np
 import pytest
@@ -24,15 +25,16 @@ def nvq():
 
 
 def _check(nvq, oracle_mod, w, dy, counts):
+    """Both sides read the rowwise copy the oracle makes of w."""
     E, out, inn = w.shape
-    q = nvq.nvfp4_quantize(w, four_over_six=True)
+    q = oracle_mod.nvfp4_quantize(u16(w), four_over_six=True)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    dx = nvq.nvfp4_dgrad(dy, counts, q["codes"], q["scales"], q["tensor_scale"], status=st)
+    dx = nvq.nvfp4_dgrad(dy, counts, torch.from_numpy(q["codes"]).cuda(),
+                         torch.from_numpy(q["scales"]).cuda(), torch.from_numpy(q["G"]).cuda(),
+                         status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    ref, bound = oracle_mod.nvfp4_dgrad(u16(dy), counts, q["codes"].cpu().numpy(),
-                                        q["scales"].cpu().numpy(), q["tensor_scale"].cpu().numpy(),
-                                        out, inn)
+    ref, bound = oracle_mod.nvfp4_dgrad(u16(dy), counts, q["codes"], q["scales"], q["G"], out, inn)
     got = dx.cpu().numpy().astype(np.float64)
     err = np.abs(got - ref)
     tol = out * 2.0 ** -23 * bound + 1e-30
@@ -91,3 +93,11 @@ def test_dgrad_status_and_empty(nvq, oracle_mod):
     dy = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     dx = nvq.nvfp4_dgrad(dy, [0, 0], q["codes"], q["scales"], q["tensor_scale"])
     assert dx.shape == (0, 256)
+    # an empty contraction (out = 0) writes zeros over whatever dX held
+    u8 = torch.uint8
+    dx0 = torch.full((5, 256), 7.0, dtype=torch.float32, device="cuda")
+    nvq.nvfp4_dgrad(torch.empty((5, 0), dtype=torch.bfloat16, device="cuda"), [2, 3],
+                    torch.empty((2, 0, 128), dtype=u8, device="cuda"),
+                    torch.empty((2, 0, 16), dtype=u8, device="cuda"), q["tensor_scale"], out=dx0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dx0).item() == 0
