@@ -274,9 +274,9 @@ NVQ_API int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp,
  *                of expert e-1 (the caller sorts tokens by expert)
  *   counts       HOST int64 [nexp]: tokens routed to each expert (>= 0)
  *   nexp         1 .. 256
- *   out, in      the weight slice is [out, in]; out % 256 == 0, in % 64 == 0
+ *   out, in      the weight slice is [out, in]; out % 256 == 0, in % 256 == 0
  *   codes        u8 [nexp, out, in/2] as nf4_quantize writes them (32-byte
- *                aligned); absmax f32 [nexp, out, in/64]
+ *                aligned); absmax f32 [nexp, out, in/64] (16-byte aligned)
  *   y            bf16 [T, out], written (zeros when in == 0)
  *   status       device int, nullable: NVQ_STATUS_TIMEOUT if a bounded wait
  *                gave up (y is then unspecified)

@@ -411,7 +411,7 @@ int nvfp4_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int64_t
                 const uint8_t* codes, const uint8_t* scales, const float* tensor_scale, float* dx,
                 int* status, nvq_stream_t stream) {
   if (nexp < 1 || nexp > nvq::kGroupedMaxExperts || out < 0 || in < 0) return NVQ_ERR_SHAPE;
-  if (out % 64 || in % 256) return NVQ_ERR_SHAPE;
+  if (out % 64 || in % 256 || nexp * out >= (1ll << 31)) return NVQ_ERR_SHAPE;
   if (!counts) return NVQ_ERR_NULL;
   int64_t T = 0;
   for (int64_t e = 0; e < nexp; e++) {
@@ -441,7 +441,7 @@ int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, in
                       int64_t in, const uint8_t* codes, const float* absmax, uint16_t* y,
                       int* status, nvq_stream_t stream) {
   if (nexp < 1 || nexp > nvq::kGroupedMaxExperts || out < 0 || in < 0) return NVQ_ERR_SHAPE;
-  if (out % 256 || in % 64) return NVQ_ERR_SHAPE;
+  if (out % 256 || in % 256) return NVQ_ERR_SHAPE;
   if (!counts) return NVQ_ERR_NULL;
   int64_t T = 0;
   for (int64_t e = 0; e < nexp; e++) {
@@ -450,7 +450,8 @@ int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, in
     if (T >= (1ll << 31)) return NVQ_ERR_SHAPE;
   }
   int64_t total;
-  if (!mul_ok(nexp, out, in, &total) || T * in >= (1ll << 40) || T * out >= (1ll << 40))
+  if (!mul_ok(nexp, out, in, &total) || T * in >= (1ll << 40) || T * out >= (1ll << 40) ||
+      nexp * out >= (1ll << 31))
     return NVQ_ERR_SHAPE;
   if (T == 0 || out == 0) return NVQ_OK;
   const bool contract = in > 0;  // in == 0: an empty contraction, Y = 0

@@ -464,10 +464,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// No legitimate wait of these kernels lasts more than milliseconds; a wait
+// still open after this long is a stall, reported instead of waited out.
+constexpr uint64_t kMaxWaitNs = 500000000ull;
+
 // Waits for the phase of `bar` with the given parity to complete, giving up
-// after `max_tries` polls (each poll may itself block for a short,
-// hardware-defined time).  Returns false on giving up.
+// after `max_tries` polls or kMaxWaitNs of wall-clock time, whichever comes
+// first (a poll may itself block for a short, hardware-defined time, so the
+// count alone does not bound the time).  Returns false on giving up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_tries) {
+  uint64_t t0 = 0;
   for (uint32_t i = 0; i < max_tries; i++) {
     uint32_t done;
     asm volatile(
@@ -478,6 +490,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     if (done) return true;
+    const uint64_t now = globaltimer_ns();
+    if (i == 0) t0 = now;
+    else if (now - t0 > kMaxWaitNs) return false;
   }
   return false;
 }

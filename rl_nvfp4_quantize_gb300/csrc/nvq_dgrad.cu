@@ -10,9 +10,10 @@
 //
 // B is the weight slice itself, W_e [out][in] = [K][N]: N-contiguous, so the
 // producers write it MN-major, in the orientation it is stored in -- no
-// transposition.  Producer warp w forms K rows 8w .. 8w+7 of each K step;
-// lane l the eight N values 8l .. 8l+7 (one code word, half a scale block), so
-// a warp's code loads cover one contiguous 128-byte run of a row.
+// transposition.  The codes and scales of each K step (64 rows x 256 columns)
+// are staged in shared memory by TMA; producer warp w forms K rows 8w .. 8w+7
+// of the step, lane l the eight N values 8l .. 8l+7 (one code word, half a
+// scale block), so a warp reads one contiguous 128-byte row of codes.
 #include <cuda.h>
 #include <cstdint>
 
@@ -24,46 +25,44 @@ namespace nvq {
 
 struct Nvfp4DgradProducer {
   struct Params {
-    const uint8_t* codes;   // [nexp, out, in/2]
-    const uint8_t* scales;  // [nexp, out, in/16]
+    CUtensorMap codes;      // [nexp * out][in/2] u8, boxes of 128 bytes x 64 rows
+    CUtensorMap scales;     // [nexp * out][in/16] u8, boxes of 16 bytes x 64 rows
     const float* G;         // [nexp]
   };
-  static constexpr int kAhead = 3;
+  // staged per K step: the codes of 64 rows x 256 columns (64 x 128 bytes),
+  // then their scales (64 x 16 bytes)
+  static constexpr int kSC = 3;
+  static constexpr int kCBytes = kGK * 128 + kGK * 16;
+  static constexpr int kCExtra = 0;
   static constexpr int kExtraSmem = 0;
   static constexpr bool kMnMajor = true;
 
-  const uint8_t* pc;  // this lane's code word in K row 8w of K step 0
-  const uint8_t* ps;  // its scale byte
-  int64_t in_h, in_16;
   float2 G2;
-  int soff;           // byte offset of this lane's chunk in row 8w of the slice (unswizzled)
-  int chunk;          // its 16-byte chunk within the 128-byte row
-  uint32_t cw[kAhead][8], sbyte[kAhead][8];
+  int coff;   // this lane's code word in K row 8w of a staged step
+  int soff;   // its scale byte
+  int toff;   // its 16-byte chunk in K row 8w of the slice (unswizzled)
+  int chunk;  // that chunk's index within the 128-byte row
 
   __device__ static void build_extra(unsigned char*) {}
 
-  __device__ __forceinline__ void setup(const Params& P, int e, int n0, int K, int N, int p,
-                                        const unsigned char*) {
-    const int w = p >> 5, l = p & 31;
-    in_h = N >> 1;
-    in_16 = N >> 4;
-    const int64_t row0 = (int64_t)e * K + 8 * w;
-    pc = P.codes + row0 * in_h + (n0 >> 1) + 4 * l;
-    ps = P.scales + row0 * in_16 + (n0 >> 4) + (l >> 1);
-    const float g = P.G[e];
-    G2 = make_float2(g, g);
-    // block of 64 N values l >> 3 (8 KiB apart), K row 8w
-    soff = (l >> 3) * (kGB / 4) + 8 * w * 128;
-    chunk = l & 7;
+  __device__ static void stage(const Params& P, int e, int n0, int K, int, int ks,
+                               unsigned char* cst, unsigned char*, uint64_t* bar) {
+    const int y = e * K + ks * kGK;
+    mbar_arrive_expect_tx(bar, kCBytes);
+    tma_load_2d(cst, &P.codes, n0 >> 1, y, bar);
+    tma_load_2d(cst + kGK * 128, &P.scales, n0 >> 4, y, bar);
   }
 
-  __device__ __forceinline__ void load(int ks, int j) {
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const int64_t r = (int64_t)ks * kGK + i;
-      cw[j][i] = __ldg(reinterpret_cast<const uint32_t*>(pc + r * in_h));
-      sbyte[j][i] = __ldg(ps + r * in_16);
-    }
+  __device__ __forceinline__ void setup(const Params& P, int e, int, int, int, int p,
+                                        const unsigned char*) {
+    const int w = p >> 5, l = p & 31;
+    const float g = P.G[e];
+    G2 = make_float2(g, g);
+    coff = 8 * w * 128 + 4 * l;
+    soff = kGK * 128 + 8 * w * 16 + (l >> 1);
+    // block of 64 N values l >> 3 (8 KiB apart), K row 8w
+    toff = (l >> 3) * (kGB / 4) + 8 * w * 128;
+    chunk = l & 7;
   }
 
   // One code word: the eight values 8l .. 8l+7 of one K row, as four bf16
@@ -74,28 +73,31 @@ struct Nvfp4DgradProducer {
     return bf16x2_rn(y.x, y.y);
   }
 
-  __device__ __forceinline__ void produce(int j, int next, unsigned char* tile) {
-    uint32_t cur[8], S2[8];
+  __device__ __forceinline__ void produce(int, const unsigned char* cst, const unsigned char*,
+                                          unsigned char* tile) const {
+    // K row 8w + i: code word at row * 128, scale byte at row * 16; in the
+    // slice it sits at (8w + i) * 128 in its block, swizzle phase i
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-      S2[i] = e4m3_to_f16x2(sbyte[j][i] & 0x7f);
-      cur[i] = cw[j][i];
+      const uint32_t c = *reinterpret_cast<const uint32_t*>(cst + coff + i * 128);
+      const uint32_t S2 = e4m3_to_f16x2(cst[soff + i * 16] & 0x7f);
+      *reinterpret_cast<uint4*>(tile + toff + i * 128 + ((chunk ^ i) << 4)) =
+          make_uint4(pair<0>(c, S2), pair<1>(c, S2), pair<2>(c, S2), pair<3>(c, S2));
     }
-    if (next >= 0) load(next, j);
-    // K row 8w + i sits at (8w + i) * 128 in its block; its swizzle phase is
-    // (8w + i) & 7 = i
-#pragma unroll
-    for (int i = 0; i < 8; i++)
-      *reinterpret_cast<uint4*>(tile + soff + i * 128 + ((chunk ^ i) << 4)) =
-          make_uint4(pair<0>(cur[i], S2[i]), pair<1>(cur[i], S2[i]), pair<2>(cur[i], S2[i]),
-                     pair<3>(cur[i], S2[i]));
   }
 };
 
 cudaError_t launch_dgrad(const uint16_t* dy, const int64_t* counts, int64_t nexp, int out, int in,
                          const uint8_t* codes, const uint8_t* scales, const float* G, float* dx,
                          int* status, cudaStream_t s) {
-  const Nvfp4DgradProducer::Params w{codes, scales, G};
+  Nvfp4DgradProducer::Params w;
+  const uint64_t rows = (uint64_t)nexp * out;
+  if (!encode_tmap_2d(&w.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)in / 2, rows,
+                      (uint64_t)in / 2, 128, kGK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap_2d(&w.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)in / 16, rows,
+                      (uint64_t)in / 16, 16, kGK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  w.G = G;
   return launch_grouped_gemm<Nvfp4DgradProducer, 4, 2, false>(dy, counts, nexp, out, in, w, dx,
                                                                 status, s);
 }

@@ -13,19 +13,21 @@
 // 64; the B slice of a K step serves both halves.  One CTA per tile, ten
 // warps:
 //   warps 0-7 : producers -- form the 256 x 64 B slice of each K step in one
-//               of SB shared stages; afterwards the epilogue (warps 0-3:
-//               token rows 0-127, warps 4-7: rows 128-255): tensor memory ->
-//               registers -> Y rows;
-//   warp 8    : TMA loads of the two X tiles [128 rows][64 K] (128-byte
-//               swizzle) into one of SA shared stages;
+//               of SB shared stages from the packed weight data of that step
+//               (codes and scales, staged by TMA in one of SC shared stages);
+//               afterwards the epilogue (warps 0-3: token rows 0-127, warps
+//               4-7: rows 128-255): tensor memory -> registers -> Y rows;
+//   warp 8    : lane 0: TMA loads of the two X tiles [128 rows][64 K]
+//               (128-byte swizzle) into one of SA shared stages; lane 1: TMA
+//               loads of the packed weight data of each K step;
 //   warp 9    : allocates all 512 columns of tensor memory (two 128 x 256
 //               FP32 accumulators), issues tcgen05.mma (M 128, N 256, K 16,
 //               bf16 x bf16 -> FP32) -- four per K step and half, the second
 //               half only when the expert has rows there -- commits them to
 //               the stages' "empty" barriers, and frees the tensor memory.
-// A and B have stage rings of their own: the X tiles come from L2 or HBM with
-// the latency of a TMA copy, the B slices from producers whose own loads run
-// several K steps ahead in registers.
+// X, the packed weight data and B have stage rings of their own, so each runs
+// as far ahead as its own buffers allow; the producers issue no global loads
+// of their own (only shared-memory reads at fixed offsets).
 // Every wait is bounded; a wait that gives up sets the status word's timeout
 // bit, and every path still reaches the tensor-memory release.
 #pragma once
@@ -70,20 +72,26 @@ __device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t saddr, uint32_t 
 }
 
 // Producer P provides:
-//   P::Params                 the weight operand (device pointers)
-//   P::kAhead                 K steps of loads in flight per producer thread
+//   P::Params                 the weight operand (tensor maps, pointers)
+//   P::kSC, P::kCBytes        stages of packed weight data and bytes per stage
+//   P::kCExtra                bytes of further staged data (kept across steps)
 //   P::kExtraSmem             bytes of shared memory of its own (tables)
 //   P::kMnMajor               true: B slices are MN-major (blocks of 64 N
 //                             values x 64 K rows, 8 KiB apart); false:
 //                             K-major (256 rows of 64 K values)
-//   static build_extra(extra) fills its shared memory (all threads)
+//   static build_extra(extra) fills its tables (all threads)
+//   static stage(params, e, n0, K, N, ks, cst, cextra, bar)
+//                             arms `bar` and issues the TMA loads of K step ks
+//                             (one thread)
 //   setup(params, e, n0, K, N, p, extra)
-//   load(ks, j)               loads of K step ks into register buffer j
-//   produce(j, next, tile)    forms the slice from buffer j into `tile`,
-//                             after issuing load(next, j) when next >= 0
+//   produce(ks, cst, cextra, tile)
+//                             forms the slice of K step ks into `tile` from
+//                             its staged data
 template <class P, int SA, int SB, bool OUT_BF16>
 struct GroupedGemm {
-  static constexpr int kSmem = SA * kGA + SB * kGB + P::kExtraSmem + 256;
+  static constexpr int kSC = P::kSC;
+  static constexpr int kSmem =
+      SA * kGA + SB * kGB + kSC * P::kCBytes + P::kCExtra + P::kExtraSmem + 256;
   static constexpr uint32_t kIdesc =
       idesc_bf16_f32(kGM, kGN) | (P::kMnMajor ? (1u << 16) : 0u);  // bit 16: B is MN-major
 };
@@ -92,14 +100,19 @@ template <class P, int SA, int SB, bool OUT_BF16>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_grouped_gemm(const __grid_constant__ GroupedGemmArgs<typename P::Params> A) {
   extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int SC = P::kSC;
   unsigned char* const sa = smem;
   unsigned char* const sb = smem + SA * kGA;
-  unsigned char* const extra = sb + SB * kGB;
+  unsigned char* const sc = sb + SB * kGB;
+  unsigned char* const cextra = sc + SC * P::kCBytes;
+  unsigned char* const extra = cextra + P::kCExtra;
   uint64_t* const full_a = reinterpret_cast<uint64_t*>(extra + P::kExtraSmem);
   uint64_t* const empty_a = full_a + SA;
   uint64_t* const full_b = empty_a + SA;
   uint64_t* const empty_b = full_b + SB;
-  uint64_t* const acc_bar = empty_b + SB;
+  uint64_t* const full_c = empty_b + SB;
+  uint64_t* const empty_c = full_c + SC;
+  uint64_t* const acc_bar = empty_c + SC;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
   constexpr uint32_t kIdesc = GroupedGemm<P, SA, SB, OUT_BF16>::kIdesc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,6 +148,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_init(&full_b[s], kGProducers / 32);
       mbar_init(&empty_b[s], 1);
     }
+    for (int s = 0; s < SC; s++) {
+      mbar_init(&full_c[s], 1);
+      mbar_init(&empty_c[s], kGProducers / 32);
+    }
     mbar_init(acc_bar, 1);
     fence_barrier_init();
   }
@@ -146,35 +163,30 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   bool ok = true;
   if (warp < 8) {
-    // ---- B producers (the loop is unrolled by kAhead so that every
-    // register buffer index is a constant)
+    // ---- B producers
     P prod;
     prod.setup(A.w, e, n0, A.K, A.N, threadIdx.x, extra);
-#pragma unroll
-    for (int j = 0; j < P::kAhead; j++)
-      if (j < nk) prod.load(j, j);
-    for (int k0 = 0; k0 < nk && ok; k0 += P::kAhead) {
-#pragma unroll
-      for (int j = 0; j < P::kAhead; j++) {
-        const int ks = k0 + j;
-        if (ok && ks < nk) {
-          const int s = ks % SB, u = ks / SB;
-          // the whole warp agrees on the wait, so the warp-wide steps below
-          // are reached by all of its lanes or by none
-          if (ks >= SB && !__all_sync(0xffffffffu, mbar_wait(&empty_b[s], (u - 1) & 1, kGWaitTries))) {
-            ok = false;
-          } else {
-            prod.produce(j, ks + P::kAhead < nk ? ks + P::kAhead : -1, sb + s * kGB);
-            fence_proxy_async_smem();  // the tensor cores read the slice through the async proxy
-            __syncwarp();              // then one arrival per warp
-            if (lane == 0) mbar_arrive(&full_b[s]);
-          }
-        }
+    for (int ks = 0; ks < nk; ks++) {
+      const int c = ks % SC, s = ks % SB;
+      // the whole warp agrees on each wait, so the warp-wide steps below are
+      // reached by all of its lanes or by none
+      if (!__all_sync(0xffffffffu, mbar_wait(&full_c[c], (ks / SC) & 1, kGWaitTries)) ||
+          (ks >= SB &&
+           !__all_sync(0xffffffffu, mbar_wait(&empty_b[s], (ks / SB - 1) & 1, kGWaitTries)))) {
+        ok = false;
+        break;
+      }
+      prod.produce(ks, sc + c * P::kCBytes, cextra, sb + s * kGB);
+      fence_proxy_async_smem();  // the tensor cores read the slice through the async proxy
+      __syncwarp();              // then one arrival per warp on each barrier
+      if (lane == 0) {
+        mbar_arrive(&full_b[s]);
+        mbar_arrive(&empty_c[c]);  // the staged data of step ks has been read
       }
     }
   } else if (warp == 8) {
-    // ---- X tiles by TMA
     if (lane == 0) {
+      // ---- X tiles by TMA
       int issued = 0;
       for (int ks = 0; ks < nk; ks++) {
         const int s = ks % SA, u = ks / SA;
@@ -190,6 +202,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (!ok) {  // let the copies already issued land before the CTA leaves
         for (int ks = max(0, issued - SA); ks < issued; ks++)
           mbar_wait(&full_a[ks % SA], (ks / SA) & 1, kGWaitTries);
+      }
+    } else if (lane == 1) {
+      // ---- packed weight data by TMA
+      int issued = 0;
+      for (int ks = 0; ks < nk; ks++) {
+        const int c = ks % SC, u = ks / SC;
+        if (ks >= SC && !mbar_wait(&empty_c[c], (u - 1) & 1, kGWaitTries)) {
+          ok = false;
+          break;
+        }
+        P::stage(A.w, e, n0, A.K, A.N, ks, sc + c * P::kCBytes, cextra, &full_c[c]);
+        issued = ks + 1;
+      }
+      if (!ok) {
+        for (int ks = max(0, issued - SC); ks < issued; ks++)
+          mbar_wait(&full_c[ks % SC], (ks / SC) & 1, kGWaitTries);
       }
     }
   } else if (warp == 9) {

@@ -10,10 +10,11 @@
 // are formed tile by tile in shared memory and never written to HBM).
 //
 // B is W_e [out][in] = [N][K]: K-contiguous, one absmax per 64 K values, so one
-// NF4 block is exactly one row of a K step.  Producer thread p forms row p of
-// the slice: 32 code bytes (one 32-byte load) and one absmax per K step.  The
-// dequantised value of each code is bf16(level[c] * absmax), the same value
-// nf4_dequant writes; a 256-entry table maps a code byte to its two levels.
+// NF4 block is exactly one row of a K step.  The codes (and absmax) of each K
+// step are staged in shared memory by TMA; producer thread p forms row p of
+// the slice from its 32 code bytes and its absmax.  The dequantised value of
+// each code is bf16(level[c] * absmax), the same value nf4_dequant writes; a
+// 256-entry table maps a code byte to its two levels.
 #include <cuda.h>
 #include <cstdint>
 
@@ -26,23 +27,25 @@ namespace nvq {
 
 struct Nf4LinearProducer {
   struct Params {
-    const uint8_t* codes;  // [nexp, out, in/2]
-    const float* absmax;   // [nexp, out, in/64]
+    CUtensorMap codes;   // [nexp * out][in/2] u8, boxes of 32 bytes x 256 rows, 32-byte swizzle
+    CUtensorMap absmax;  // [nexp * out][in/64] f32, boxes of 4 values x 256 rows
   };
-  static constexpr int kAhead = 3;
+  // staged per K step: the codes of 256 rows x 64 K values (256 x 32 bytes);
+  // every fourth step also the absmax of the next four steps (256 x 16 bytes)
+  // into one of two slots kept across steps
+  static constexpr int kSC = 3;
+  static constexpr int kCBytes = kGN * 32;
+  static constexpr int kCExtra = 2 * kGN * 16;
   // the byte -> (level[low nibble], level[high nibble]) table, replicated 16
   // times: entry b of copy l at (16 b + l) * 8 bytes; lane l reads copy l & 15,
   // so a half warp never shares a bank whatever bytes it looks up
   static constexpr int kExtraSmem = 256 * 16 * 8;
   static constexpr bool kMnMajor = false;
 
-  const uint8_t* pc;
-  const float* pa;
   const float2* tbl;
-  int roff;  // byte offset of this thread's row in the slice
+  int p;     // this thread's row of the slice
+  int roff;  // byte offset of that row in the slice
   int phase; // its swizzle phase (row & 7)
-  uint32_t cw[kAhead][8];
-  float am[kAhead];
 
   __device__ static void build_extra(unsigned char* extra) {
     float2* t = reinterpret_cast<float2*>(extra);
@@ -52,19 +55,21 @@ struct Nf4LinearProducer {
     }
   }
 
-  __device__ __forceinline__ void setup(const Params& P, int e, int n0, int K, int N, int p,
+  __device__ static void stage(const Params& P, int e, int n0, int, int N, int ks,
+                               unsigned char* cst, unsigned char* cextra, uint64_t* bar) {
+    const int y = e * N + n0;
+    const bool am = (ks & 3) == 0;
+    mbar_arrive_expect_tx(bar, kCBytes + (am ? kGN * 16 : 0));
+    tma_load_2d(cst, &P.codes, ks * 32, y, bar);
+    if (am) tma_load_2d(cextra + ((ks >> 2) & 1) * (kGN * 16), &P.absmax, ks, y, bar);
+  }
+
+  __device__ __forceinline__ void setup(const Params&, int, int, int, int, int pp,
                                         const unsigned char* extra) {
-    const int64_t row = (int64_t)e * N + n0 + p;
-    pc = P.codes + row * (K >> 1);
-    pa = P.absmax + row * (K >> 6);
+    p = pp;
     tbl = reinterpret_cast<const float2*>(extra) + (p & 15);
     roff = p * 128;
     phase = p & 7;
-  }
-
-  __device__ __forceinline__ void load(int ks, int j) {
-    ldg32(pc + (int64_t)ks * 32, cw[j]);
-    am[j] = __ldg(pa + ks);
   }
 
   __device__ __forceinline__ uint32_t pair(uint32_t byte, float2 a2) const {
@@ -72,26 +77,36 @@ struct Nf4LinearProducer {
     return bf16x2_rn(y.x, y.y);
   }
 
-  __device__ __forceinline__ void produce(int j, int next, unsigned char* tile) {
-    uint32_t cur[8];
-#pragma unroll
-    for (int c = 0; c < 8; c++) cur[c] = cw[j][c];
-    const float2 a2 = make_float2(am[j], am[j]);
-    if (next >= 0) load(next, j);
+  __device__ __forceinline__ void produce(int ks, const unsigned char* cst,
+                                          const unsigned char* cextra, unsigned char* tile) const {
+    // row p's 32 code bytes: two 16-byte chunks, swapped on rows with bit 2
+    // set (the 32-byte swizzle); its absmax: value ks & 3 of its 16-byte row
+    const int sw = (p >> 2) & 1;
+    const uint4 lo = *reinterpret_cast<const uint4*>(cst + p * 32 + (sw << 4));
+    const uint4 hi = *reinterpret_cast<const uint4*>(cst + p * 32 + ((sw ^ 1) << 4));
+    const float a = reinterpret_cast<const float*>(cextra + ((ks >> 2) & 1) * (kGN * 16))[p * 4 + (ks & 3)];
+    const float2 a2 = make_float2(a, a);
+    const uint32_t cw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     // word c holds the codes of K values 8c .. 8c+7 (code 2b in the low
     // nibble of byte b): one 16-byte chunk of the row, swizzled by phase
 #pragma unroll
     for (int c = 0; c < 8; c++)
       *reinterpret_cast<uint4*>(tile + roff + ((c ^ phase) << 4)) =
-          make_uint4(pair(cur[c] & 0xffu, a2), pair((cur[c] >> 8) & 0xffu, a2),
-                     pair((cur[c] >> 16) & 0xffu, a2), pair(cur[c] >> 24, a2));
+          make_uint4(pair(cw[c] & 0xffu, a2), pair((cw[c] >> 8) & 0xffu, a2),
+                     pair((cw[c] >> 16) & 0xffu, a2), pair(cw[c] >> 24, a2));
   }
 };
 
 cudaError_t launch_nf4_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, int out,
                               int in, const uint8_t* codes, const float* absmax, uint16_t* y,
                               int* status, cudaStream_t s) {
-  const Nf4LinearProducer::Params w{codes, absmax};
+  Nf4LinearProducer::Params w;
+  const uint64_t rows = (uint64_t)nexp * out;
+  if (!encode_tmap_2d(&w.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)in / 2, rows,
+                      (uint64_t)in / 2, 32, kGN, CU_TENSOR_MAP_SWIZZLE_32B) ||
+      !encode_tmap_2d(&w.absmax, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, absmax, (uint64_t)in / 64, rows,
+                      (uint64_t)in / 16, 4, kGN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   return launch_grouped_gemm<Nf4LinearProducer, 3, 2, true>(x, counts, nexp, in, out, w, y,
                                                              status, s);
 }

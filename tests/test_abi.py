@@ -123,15 +123,15 @@ def test_validation_before_any_device_work(nvq):
     zero = (C.c_int64 * 2)(0, 0)
     assert L.nvfp4_dgrad(P, C.cast(zero, C.c_void_p), 2, 64, 256, P, P, P, P, P, P) == 0
     assert L.nf4_routed_linear(ok16, cntp, 2, 200, 64, ok16, ok16, ok16, P, P) == 3   # out % 256
-    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 96, ok16, ok16, ok16, P, P) == 3   # in % 64
-    assert L.nf4_routed_linear(ok16, cntp, 300, 256, 64, ok16, ok16, ok16, P, P) == 3  # > 256 experts
-    assert L.nf4_routed_linear(ok16, C.cast(neg, C.c_void_p), 2, 256, 64, ok16, ok16, ok16, P, P) == 3
-    assert L.nf4_routed_linear(ok16, P, 2, 256, 64, ok16, ok16, ok16, P, P) == 1
-    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 64, ok16, ok16, P, P, P) == 1
-    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 64, P, ok16, ok16, P, P) == 1
-    assert L.nf4_routed_linear(mis, cntp, 2, 256, 64, ok16, ok16, ok16, P, P) == 2
-    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 64, _vp(FAKE + 16), ok16, ok16, P, P) == 2  # codes % 32
-    assert L.nf4_routed_linear(P, C.cast(zero, C.c_void_p), 2, 256, 64, P, P, P, P, P) == 0
+    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 192, ok16, ok16, ok16, P, P) == 3  # in % 256
+    assert L.nf4_routed_linear(ok16, cntp, 300, 256, 256, ok16, ok16, ok16, P, P) == 3  # > 256 experts
+    assert L.nf4_routed_linear(ok16, C.cast(neg, C.c_void_p), 2, 256, 256, ok16, ok16, ok16, P, P) == 3
+    assert L.nf4_routed_linear(ok16, P, 2, 256, 256, ok16, ok16, ok16, P, P) == 1
+    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 256, ok16, ok16, P, P, P) == 1
+    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 256, P, ok16, ok16, P, P) == 1
+    assert L.nf4_routed_linear(mis, cntp, 2, 256, 256, ok16, ok16, ok16, P, P) == 2
+    assert L.nf4_routed_linear(ok16, cntp, 2, 256, 256, _vp(FAKE + 16), ok16, ok16, P, P) == 2  # codes % 32
+    assert L.nf4_routed_linear(P, C.cast(zero, C.c_void_p), 2, 256, 256, P, P, P, P, P) == 0
     assert L.nvfp4_dgrad(P, cntp, 2, 0, 256, P, P, P, P, P, P) == 1   # out == 0 still needs dX
     assert L.nvq_debug_wait_timeout(0, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3

@@ -61,19 +61,19 @@ def _check(nvq, oracle_mod, E, out, inn, counts, seed):
 
 
 @pytest.mark.parametrize("E,out,inn,counts", [
-    (1, 256, 64, [128]),      # one tile, one K step
-    (1, 256, 128, [1]),       # one token
-    (1, 512, 256, [300]),     # two token tiles (ragged), two column tiles, four K steps
+    (1, 256, 256, [128]),     # one tile, four K steps (one absmax fetch)
+    (1, 256, 256, [1]),       # one token
+    (1, 512, 512, [300]),     # two token tiles (ragged), two column tiles, eight K steps
 ])
 def test_nf4_linear_tiny(nvq, oracle_mod, E, out, inn, counts):
     _check(nvq, oracle_mod, E, out, inn, counts, seed=out + inn)
 
 
 @pytest.mark.parametrize("E,out,inn,counts", [
-    (3, 256, 128, [5, 0, 130]),
+    (3, 256, 256, [5, 0, 130]),
     (2, 512, 512, [200, 77]),
-    (4, 512, 384, [129, 128, 0, 300]),
-    (5, 768, 1024, [64, 1, 255, 256, 257]),
+    (4, 512, 768, [129, 128, 0, 300]),
+    (5, 768, 1280, [64, 1, 255, 256, 257]),
 ])
 def test_nf4_linear_grouped_ragged(nvq, oracle_mod, E, out, inn, counts):
     _check(nvq, oracle_mod, E, out, inn, counts, seed=out * 3 + inn)
@@ -98,9 +98,9 @@ def test_nf4_linear_exact_values_bit_identical(nvq, oracle_mod):
 
 
 def test_nf4_linear_empty_and_zero_k(nvq):
-    codes = torch.zeros((2, 256, 32), dtype=torch.uint8, device="cuda")
-    absmax = torch.ones((2, 256, 1), dtype=torch.float32, device="cuda")
-    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    codes = torch.zeros((2, 256, 128), dtype=torch.uint8, device="cuda")
+    absmax = torch.ones((2, 256, 4), dtype=torch.float32, device="cuda")
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
     y = nvq.nf4_routed_linear(x, [0, 0], codes, absmax)
     assert y.shape == (0, 256)
     # an empty contraction writes zeros over whatever the output held
