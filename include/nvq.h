@@ -24,7 +24,8 @@
  *    ([P5] "Why every quantizer misses 95% of the model").
  *  - Packing.  Two 4-bit codes per byte, element 2j in the low nibble and
  *    element 2j+1 in the high nibble.  Block scales are one byte per block,
- *    stored linearly (row-major over blocks, no swizzle).
+ *    stored linearly (row-major over blocks), unless NVQ_SCALES_SWIZZLED
+ *    selects the tensor-core tiled layout.
  *  - Asynchrony.  A call validates its arguments on the host, enqueues its
  *    kernels on `stream` and returns.  The return value reports only what is
  *    known at that point: a validation error (no work is enqueued) or a
@@ -79,7 +80,21 @@ enum nvq_flags {
   NVQ_4OVER6 = 1u << 0,
   /* amax[] is an input (the caller's per-slice absolute maximum) instead of
      being computed; lets a caller skip the reduction pass.                 */
-  NVQ_AMAX_GIVEN = 1u << 1
+  NVQ_AMAX_GIVEN = 1u << 1,
+  /* Block scales are written in the tensor-core tiled layout the
+     block-scaled FP4 GEMM reads ([P1] "Why can't we just transpose the one
+     copy?": the scales are "swizzled" for the tensor-core tile) instead of
+     linearly.  For a [R, C] matrix of block scales (R quantised rows, C =
+     blocks per row): R is padded to a multiple of 128, C to a multiple of 4;
+     tiles of 128 rows x 4 block columns (512 bytes) follow one another
+     row-major (ceil(C/4) tiles per tile row); inside a tile, scale (r, c)
+     sits at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.  Padding
+     entries are 0.  Each expert slice occupies nvq_scale_bytes(R, 16 C,
+     NVQ_SCALES_SWIZZLED) bytes.  Codes are unchanged.  Accepted by
+     nvfp4_quantize, nvfp4_quantize_dual (both copies) and
+     act_quantize_per_token; the dequantising and GEMM calls of this library
+     read the linear layout.                                                */
+  NVQ_SCALES_SWIZZLED = 1u << 2
 };
 
 /* Bits of the device status word. */
@@ -93,6 +108,12 @@ enum nvq_device_status {
      then unspecified and the device stays usable. */
   NVQ_STATUS_TIMEOUT = 4
 };
+
+/* Bytes of the block scales of one [rows, cols] slice (cols % 16 == 0) in
+   the layout `flags` selects: rows * cols / 16 linearly, or the padded size
+   of the tiled layout with NVQ_SCALES_SWIZZLED.  -1 for invalid arguments.
+   Host only; needs no device. */
+NVQ_API int64_t nvq_scale_bytes(int64_t rows, int64_t cols, unsigned flags);
 
 /* Library version, (major << 16) | minor. */
 NVQ_API int nvq_version(void);
@@ -116,7 +137,9 @@ NVQ_API const char* nvq_status_string(int code);
  *
  *   w        in   bf16 [nexp, rows, cols]; cols % 16 == 0
  *   codes    out  u8   [nexp, rows, cols/2]
- *   scales   out  u8   [nexp, rows, cols/16]  E4M3 bytes
+ *   scales   out  u8   [nexp, rows, cols/16]  E4M3 bytes (with
+ *            NVQ_SCALES_SWIZZLED: nexp slices of nvq_scale_bytes(rows, cols,
+ *            NVQ_SCALES_SWIZZLED) bytes in the tiled layout)
  *   amax     in/out f32 [nexp]  (input iff NVQ_AMAX_GIVEN; empty slices give 0)
  *   tensor_scale out f32 [nexp] G_e
  *   status   out  device int, nullable (with NVQ_AMAX_GIVEN the input is not
@@ -137,6 +160,8 @@ NVQ_API int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_
  *   w           in   bf16 [nexp, out, in]; out % 16 == 0, in % 16 == 0
  *   codes_row   out  u8 [nexp, out, in/2]     scales_row out u8 [nexp, out, in/16]
  *   codes_col   out  u8 [nexp, in, out/2]     scales_col out u8 [nexp, in, out/16]
+ *   (with NVQ_SCALES_SWIZZLED each scale buffer holds nexp tiled slices of
+ *   nvq_scale_bytes(out, in, .) resp. nvq_scale_bytes(in, out, .) bytes)
  *   amax, tensor_scale, status as in nvfp4_quantize
  */
 NVQ_API int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in,
@@ -181,7 +206,9 @@ NVQ_API int nvfp4_dequant_t(const uint8_t* codes_row, const uint8_t* scales_row,
  * the row as the slice.
  *
  *   x in bf16 [T, H], H % 16 == 0; codes out u8 [T, H/2];
- *   scales out u8 [T, H/16]; token_scale out f32 [T]; flags: NVQ_4OVER6 only
+ *   scales out u8 [T, H/16] (with NVQ_SCALES_SWIZZLED: nvq_scale_bytes(T,
+ *   H, .) bytes in the tiled layout); token_scale out f32 [T];
+ *   flags: NVQ_4OVER6, NVQ_SCALES_SWIZZLED
  */
 NVQ_API int act_quantize_per_token(const uint16_t* x, int64_t T, int64_t H, unsigned flags,
                            uint8_t* codes, uint8_t* scales, float* token_scale,

@@ -369,3 +369,50 @@ def nf4_routed_linear(x: np.ndarray, counts, codes: np.ndarray, absmax: np.ndarr
         t0 += c
     return y, bound
 
+
+def scales_tiled(scales: np.ndarray) -> np.ndarray:
+    """Block scales [..., R, C] (linear: row r, block column c) -> [..., Rp * Cp]
+    in the tensor-core tiled layout the block-scaled FP4 GEMM reads ("Getting
+    GLM-5.2 NVFP4 Post-Training off the ground", "Why can't we just transpose
+    the one copy?": the scales are swizzled for the tensor-core tile; the
+    pages do not spell the layout out, so this is the published layout of
+    the FP4 GEMM's scale operand).  Rp = R rounded up to 128, Cp = C rounded
+    up to 4; tiles of 128 rows x 4 block columns, 512 bytes each, row-major
+    over tiles; inside a tile scale (r, c) at byte (r % 32) * 16 +
+    ((r // 32) % 4) * 4 + c % 4; padding 0.  Parity: pinned on the GPU by
+    the FP4 GEMM that consumes the layout; on the host only its bijection,
+    tile grouping and padding are checked."""
+    scales = np.ascontiguousarray(scales, np.uint8)
+    *lead, R, C = scales.shape
+    Rp, Cp = -(-R // 128) * 128, -(-C // 4) * 4
+    r = np.arange(R)[:, None]
+    c = np.arange(C)[None, :]
+    off = ((r // 128) * (Cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + c % 4
+    out = np.zeros(tuple(lead) + (Rp * Cp,), np.uint8)
+    out[..., off] = scales
+    return out
+
+
+def nvfp4_block_values(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """c * S of every element, float64 and exact (an E2M1 value times an E4M3
+    value has at most six significant bits): the operand values of a
+    block-scaled FP4 product before any FP32 tensor or token scale.
+    codes [..., R, K/2] (element 2j in the low nibble of byte j), scales
+    [..., R, K/16] linear."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    e2 = np.array([e2m1_value(c) for c in range(16)], np.float64)
+    e4 = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    nib = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), np.uint8)
+    nib[..., 0::2] = codes & 0xF
+    nib[..., 1::2] = codes >> 4
+    return e2[nib] * np.repeat(e4[scales], 16, axis=-1)
+
+
+def nvfp4_scaled_product(a_codes, a_scales, b_codes, b_scales):
+    """Y[m, n] = sum_k (c S)_a[m, k] (c S)_b[n, k] in float64 -- the product a
+    block-scaled FP4 GEMM forms from two NVFP4 operands with K-major codes --
+    and bound = sum_k |(c S)_a (c S)_b|."""
+    va = nvfp4_block_values(a_codes, a_scales)
+    vb = nvfp4_block_values(b_codes, b_scales)
+    return va @ vb.T, np.abs(va) @ np.abs(vb).T

@@ -22,14 +22,15 @@ import os
 import torch
 
 __all__ = [
-    "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
+    "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "FLAG_SCALES_SWIZZLED", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
     "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t", "nvfp4_dgrad",
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed", "nf4_routed_linear",
-    "nf4_codebook", "debug_convert", "debug_wait_timeout", "lib", "library_path",
+    "nf4_codebook", "scale_bytes", "debug_convert", "debug_wait_timeout", "lib", "library_path",
 ]
 
 FLAG_4OVER6 = 1
 FLAG_AMAX_GIVEN = 2
+FLAG_SCALES_SWIZZLED = 4
 STATUS_NONFINITE = 1
 STATUS_BAD_INDEX = 2
 STATUS_TIMEOUT = 4
@@ -54,6 +55,7 @@ def _load():
     sig = {
         "nvq_version": ([], i32),
         "nvq_status_string": ([i32], C.c_char_p),
+        "nvq_scale_bytes": ([i64, i64, u32], i64),
         "nvfp4_quantize": ([P, i64, i64, i64, u32, P, P, P, P, P, P], i32),
         "nvfp4_quantize_dual": ([P, i64, i64, i64, u32, P, P, P, P, P, P, P, P], i32),
         "nvfp4_dequant": ([P, P, P, i64, i64, i64, P, P], i32),
@@ -115,36 +117,58 @@ def _empty(shape, dtype, like):
 
 # ---------------------------------------------------------------- NVFP4
 
-def nvfp4_quantize(w, four_over_six=False, amax=None, status=None, stream=None, out=None):
+def scale_bytes(rows, cols, swizzled=False):
+    """Bytes of the block scales of one [rows, cols] slice (see
+    nvq_scale_bytes in nvq.h)."""
+    n = lib.nvq_scale_bytes(rows, cols, FLAG_SCALES_SWIZZLED if swizzled else 0)
+    if n < 0:
+        raise ValueError("invalid scale shape [%d, %d]" % (rows, cols))
+    return n
+
+
+def _scales(E, R, K, swizzled, like):
+    """Block-scale buffer: [E, R, K/16] linear, or [E, bytes] tiled."""
+    if swizzled:
+        return _empty((E, scale_bytes(R, K, True)), torch.uint8, like)
+    return _empty((E, R, K // 16), torch.uint8, like)
+
+
+def nvfp4_quantize(w, four_over_six=False, amax=None, status=None, stream=None, out=None,
+                   swizzled_scales=False):
     """Rowwise NVFP4 of w [nexp, rows, cols] (bf16).  Returns a dict with
-    codes [nexp, rows, cols/2] u8, scales [nexp, rows, cols/16] u8 (E4M3),
-    amax [nexp] f32 and tensor_scale [nexp] f32."""
+    codes [nexp, rows, cols/2] u8, scales [nexp, rows, cols/16] u8 (E4M3; with
+    swizzled_scales [nexp, scale_bytes(rows, cols, True)] in the tensor-core
+    tiled layout), amax [nexp] f32 and tensor_scale [nexp] f32."""
     w = _as3d(_bf16(w, "w"))
     E, R, K = w.shape
     o = out or {}
     codes = o.get("codes", _empty((E, R, K // 2), torch.uint8, w))
-    scales = o.get("scales", _empty((E, R, K // 16), torch.uint8, w))
+    scales = o.get("scales") if "scales" in o else _scales(E, R, K, swizzled_scales, w)
     am = amax if amax is not None else o.get("amax", _empty((E,), torch.float32, w))
     G = o.get("tensor_scale", _empty((E,), torch.float32, w))
-    flags = (FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
+    flags = ((FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
+             | (FLAG_SCALES_SWIZZLED if swizzled_scales else 0))
     _check("nvfp4_quantize", lib.nvfp4_quantize(_ptr(w), E, R, K, flags, _ptr(codes), _ptr(scales),
                                                 _ptr(am), _ptr(G), _ptr(status), _stream(stream)))
     return dict(codes=codes, scales=scales, amax=am, tensor_scale=G)
 
 
-def nvfp4_quantize_dual(w, four_over_six=True, amax=None, status=None, stream=None, out=None):
+def nvfp4_quantize_dual(w, four_over_six=True, amax=None, status=None, stream=None, out=None,
+                        swizzled_scales=False):
     """Rowwise and columnwise NVFP4 of w [nexp, out, in] from one read.
-    Columnwise outputs are K-major for dgrad: [nexp, in, out/2] / [nexp, in, out/16]."""
+    Columnwise outputs are K-major for dgrad: [nexp, in, out/2] / [nexp, in, out/16]
+    (scales [nexp, scale_bytes(in, out, True)] with swizzled_scales)."""
     w = _as3d(_bf16(w, "w"))
     E, R, K = w.shape
     o = out or {}
     cr = o.get("codes_row", _empty((E, R, K // 2), torch.uint8, w))
-    sr = o.get("scales_row", _empty((E, R, K // 16), torch.uint8, w))
+    sr = o.get("scales_row") if "scales_row" in o else _scales(E, R, K, swizzled_scales, w)
     cc = o.get("codes_col", _empty((E, K, R // 2), torch.uint8, w))
-    sc = o.get("scales_col", _empty((E, K, R // 16), torch.uint8, w))
+    sc = o.get("scales_col") if "scales_col" in o else _scales(E, K, R, swizzled_scales, w)
     am = amax if amax is not None else o.get("amax", _empty((E,), torch.float32, w))
     G = o.get("tensor_scale", _empty((E,), torch.float32, w))
-    flags = (FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
+    flags = ((FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
+             | (FLAG_SCALES_SWIZZLED if swizzled_scales else 0))
     _check("nvfp4_quantize_dual",
            lib.nvfp4_quantize_dual(_ptr(w), E, R, K, flags, _ptr(cr), _ptr(sr), _ptr(cc), _ptr(sc),
                                    _ptr(am), _ptr(G), _ptr(status), _stream(stream)))
@@ -172,17 +196,24 @@ def nvfp4_dequant_t(codes_row, scales_row, tensor_scale, stream=None, out=None):
     return dst
 
 
-def act_quantize_per_token(x, four_over_six=True, status=None, stream=None, out=None):
-    """NVFP4 activations [T, H] with one FP32 scale per token."""
+def act_quantize_per_token(x, four_over_six=True, status=None, stream=None, out=None,
+                           swizzled_scales=False):
+    """NVFP4 activations [T, H] with one FP32 scale per token (scales
+    [scale_bytes(T, H, True)] in the tiled layout with swizzled_scales)."""
     x = _bf16(x, "x")
     if x.dim() != 2:
         raise ValueError("expected x [T, H]")
     T, H = x.shape
     o = out or {}
     codes = o.get("codes", _empty((T, H // 2), torch.uint8, x))
-    scales = o.get("scales", _empty((T, H // 16), torch.uint8, x))
+    if "scales" in o:
+        scales = o["scales"]
+    elif swizzled_scales:
+        scales = _empty((scale_bytes(T, H, True),), torch.uint8, x)
+    else:
+        scales = _empty((T, H // 16), torch.uint8, x)
     ts = o.get("token_scale", _empty((T,), torch.float32, x))
-    flags = FLAG_4OVER6 if four_over_six else 0
+    flags = (FLAG_4OVER6 if four_over_six else 0) | (FLAG_SCALES_SWIZZLED if swizzled_scales else 0)
     _check("act_quantize_per_token",
            lib.act_quantize_per_token(_ptr(x), T, H, flags, _ptr(codes), _ptr(scales), _ptr(ts),
                                       _ptr(status), _stream(stream)))

@@ -223,10 +223,26 @@ const char* nvq_status_string(int code) {
   }
 }
 
+// The tiled layout pads rows to a multiple of 128 and blocks per row to a
+// multiple of 4; the kernels write only the real entries, so a ragged shape
+// first zeroes the whole buffer (the common, unpadded shapes skip this).
+static int zero_tiled_padding(uint8_t* scales, int64_t nexp, int64_t rows, int64_t cols,
+                              cudaStream_t s) {
+  if (rows % 128 == 0 && (cols / 16) % 4 == 0) return NVQ_OK;
+  return launch_result(cudaMemsetAsync(
+      scales, 0, (size_t)(nexp * nvq::tiled_scale_bytes(rows, cols)), s));
+}
+
+int64_t nvq_scale_bytes(int64_t rows, int64_t cols, unsigned flags) {
+  if (rows < 0 || cols < 0 || cols % 16 || (flags & ~(unsigned)NVQ_SCALES_SWIZZLED)) return -1;
+  if (rows > (1ll << 40) || cols > (1ll << 40)) return -1;
+  return (flags & NVQ_SCALES_SWIZZLED) ? nvq::tiled_scale_bytes(rows, cols) : rows * (cols / 16);
+}
+
 int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, unsigned flags,
                    uint8_t* codes, uint8_t* scales, float* amax, float* tensor_scale, int* status,
                    nvq_stream_t stream) {
-  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_AMAX_GIVEN)) return NVQ_ERR_FLAGS;
+  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_AMAX_GIVEN | NVQ_SCALES_SWIZZLED)) return NVQ_ERR_FLAGS;
   int64_t total;
   int rc = check_stack(nexp, rows, cols, &total);
   if (rc) return rc;
@@ -243,18 +259,20 @@ int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, 
   cudaStream_t s = cs(stream);
   const bool f46 = flags & NVQ_4OVER6;
   const bool given = flags & NVQ_AMAX_GIVEN;
+  const bool tiled = flags & NVQ_SCALES_SWIZZLED;
   if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
   if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
+  if (tiled && (rc = zero_tiled_padding(scales, nexp, rows, cols, s))) return rc;
   return launch_result(nvq::launch_quant_tiles(w, nexp, (int)rows, (int)cols, f46, codes, scales,
                                                nullptr, nullptr, amax, tensor_scale, status,
-                                               !given, s));
+                                               !given, tiled, s));
 }
 
 int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in, unsigned flags,
                         uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
                         uint8_t* scales_col, float* amax, float* tensor_scale, int* status,
                         nvq_stream_t stream) {
-  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_AMAX_GIVEN)) return NVQ_ERR_FLAGS;
+  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_AMAX_GIVEN | NVQ_SCALES_SWIZZLED)) return NVQ_ERR_FLAGS;
   int64_t total;
   int rc = check_stack(nexp, out, in, &total);
   if (rc) return rc;
@@ -273,11 +291,15 @@ int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in
   cudaStream_t s = cs(stream);
   const bool f46 = flags & NVQ_4OVER6;
   const bool given = flags & NVQ_AMAX_GIVEN;
+  const bool tiled = flags & NVQ_SCALES_SWIZZLED;
   if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
   if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
+  if (tiled && ((rc = zero_tiled_padding(scales_row, nexp, out, in, s)) ||
+                (rc = zero_tiled_padding(scales_col, nexp, in, out, s))))
+    return rc;
   return launch_result(nvq::launch_quant_tiles(w, nexp, (int)out, (int)in, f46, codes_row,
                                                scales_row, codes_col, scales_col, amax,
-                                               tensor_scale, status, !given, s));
+                                               tensor_scale, status, !given, tiled, s));
 }
 
 int nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
@@ -314,7 +336,7 @@ int nvfp4_dequant_t(const uint8_t* codes_row, const uint8_t* scales_row, const f
 int act_quantize_per_token(const uint16_t* x, int64_t T, int64_t H, unsigned flags,
                            uint8_t* codes, uint8_t* scales, float* token_scale, int* status,
                            nvq_stream_t stream) {
-  if (flags & ~(unsigned)NVQ_4OVER6) return NVQ_ERR_FLAGS;
+  if (flags & ~(unsigned)(NVQ_4OVER6 | NVQ_SCALES_SWIZZLED)) return NVQ_ERR_FLAGS;
   int64_t total;
   int rc = check_stack(1, T, H, &total);
   if (rc) return rc;
@@ -329,8 +351,10 @@ int act_quantize_per_token(const uint16_t* x, int64_t T, int64_t H, unsigned fla
   if ((rc = device_check())) return rc;
   cudaStream_t s = cs(stream);
   if (H == 0) return launch_result(nvq::launch_zero_f32(token_scale, T, s));
+  const bool tiled = flags & NVQ_SCALES_SWIZZLED;
+  if (tiled && (rc = zero_tiled_padding(scales, 1, T, H, s))) return rc;
   return launch_result(nvq::launch_act(x, T, (int)H, (flags & NVQ_4OVER6) != 0, codes, scales,
-                                       token_scale, status, s));
+                                       token_scale, status, tiled, s));
 }
 
 int nf4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, uint8_t* codes,

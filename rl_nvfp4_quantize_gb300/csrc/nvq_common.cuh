@@ -418,6 +418,16 @@ __device__ __forceinline__ void quant_col_pair(const uint32_t wc[16], float E, c
   }
 }
 
+// ------------------------------------------------------- tiled scale layout
+// Byte offset of block scale (r, c) -- row r of the quantised matrix, block
+// column c -- in the tensor-core layout of block scales: tiles of 128 rows x
+// 4 block columns (512 bytes), row-major over tiles with `ctiles` tiles per
+// tile row; inside a tile, row r sits at (r % 32) * 16 + ((r / 32) % 4) * 4
+// and column c at c % 4.
+__device__ __forceinline__ int64_t scale_off_tiled(int64_t r, int c, int ctiles) {
+  return ((r >> 7) * ctiles + (c >> 2)) * 512 + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (c & 3);
+}
+
 // ------------------------------------------------------------ small helpers
 // Unsigned division by a divisor fixed at launch, for dividends below 2^31:
 // n / d = (umulhi(n, m) + n) >> s with s = ceil(log2 d) and

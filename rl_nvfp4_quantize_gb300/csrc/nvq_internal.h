@@ -54,13 +54,23 @@ cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, floa
 // With compute_amax the per-slice amax (zeroed by the caller) is reduced
 // here: the first chunk of slices by a reduction pass, every later chunk
 // inside the launch that quantises the chunk before it.
+// Bytes of the block scales of one [rows, cols] slice in the tensor-core
+// tiled layout: rows padded to a multiple of 128, blocks per row (cols / 16)
+// to a multiple of 4.
+inline int64_t tiled_scale_bytes(int64_t rows, int64_t cols) {
+  return (rows + 127) / 128 * 128 * ((cols / 16 + 3) / 4 * 4);
+}
+
+// With tiled, the block scales are written in the tensor-core tiled layout
+// (padding entries are the caller's to zero).
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
                                uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
                                uint8_t* scales_col, float* amax, float* tensor_scale,
-                               int* status, bool compute_amax, cudaStream_t s);
+                               int* status, bool compute_amax, bool tiled, cudaStream_t s);
 
 cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* codes,
-                       uint8_t* scales, float* token_scale, int* status, cudaStream_t s);
+                       uint8_t* scales, float* token_scale, int* status, bool tiled,
+                       cudaStream_t s);
 
 cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const float* G,
                            int64_t nexp, int64_t per_slice, uint16_t* dst, cudaStream_t s);

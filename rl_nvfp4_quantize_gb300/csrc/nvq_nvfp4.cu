@@ -151,6 +151,9 @@ struct __align__(64) QuantTileArgs {
   uint32_t ahead;         // > 0: also reduce the amax of slice e + ahead (0: off)
   const uint16_t* w;      // the stack (for the look-ahead amax reads)
   float* amax_out;        // the look-ahead amax accumulators (same array as amax)
+  int tiled;              // block scales in the tensor-core tiled layout
+  int ct_row, ct_col;     // tiled layout: tiles per tile row (rowwise, columnwise)
+  int64_t sl_row, sl_col; // tiled layout: bytes per slice (rowwise, columnwise)
 };
 
 template <bool F46, bool DUAL>
@@ -282,7 +285,11 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
           uint32_t c0w, c1w, sb;
           quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
           *reinterpret_cast<uint2*>(pc + 16 * k * cols_h) = make_uint2(c0w, c1w);
-          ps[16 * k * cols_16] = (uint8_t)sb;
+          if (A.tiled)
+            A.scales_row[T.e * A.sl_row +
+                         scale_off_tiled(T.r0 + r, (T.c0 >> 4) + cb, A.ct_row)] = (uint8_t)sb;
+          else
+            ps[16 * k * cols_16] = (uint8_t)sb;
         }
       }
     }
@@ -344,7 +351,19 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
             *reinterpret_cast<uint2*>(dstc + rb * 8) =
                 *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + c * 8);
         }
-        if (nrb == 4 && (rows & 63) == 0) {
+        if (A.tiled) {
+          // the tile's four row blocks are block columns r0/16 .. +3, a
+          // multiple of 4: four consecutive bytes of one tiled row
+          uint8_t* dt = A.scales_col + T.e * A.sl_col +
+                        scale_off_tiled(T.c0 + c, T.r0 >> 4, A.ct_col);
+          if (nrb == 4) {
+            *reinterpret_cast<uint32_t*>(dt) =
+                (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
+                ((uint32_t)cols_s[2 * kTC + c] << 16) | ((uint32_t)cols_s[3 * kTC + c] << 24);
+          } else {
+            for (int rb = 0; rb < nrb; rb++) dt[rb] = cols_s[rb * kTC + c];
+          }
+        } else if (nrb == 4 && (rows & 63) == 0) {
           const uint32_t sc = (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
                               ((uint32_t)cols_s[2 * kTC + c] << 16) |
                               ((uint32_t)cols_s[3 * kTC + c] << 24);
@@ -373,7 +392,7 @@ static cudaError_t set_quant_smem() {
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
                                uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
                                uint8_t* scales_col, float* amax, float* tensor_scale,
-                               int* status, bool compute_amax, cudaStream_t s) {
+                               int* status, bool compute_amax, bool tiled, cudaStream_t s) {
   const DevInfo* di = device_info();
   const int tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
   const int64_t per = (int64_t)tiles_r * tiles_c;
@@ -403,6 +422,11 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
   make_fastdiv((uint32_t)tiles_c, &A.by_tiles_c.m, &A.by_tiles_c.s);
   A.nexp = (uint32_t)nexp;
   A.w = w;
+  A.tiled = tiled ? 1 : 0;
+  A.ct_row = (cols / 16 + 3) / 4;
+  A.ct_col = (rows / 16 + 3) / 4;
+  A.sl_row = tiled_scale_bytes(rows, cols);
+  A.sl_col = tiled_scale_bytes(cols, rows);
   const int full_grid = di->sms * NVQ_QT_MINB;
   // Slices per launch: with the look-ahead amax every launch quantises one
   // chunk while reducing the amax of the next, so each launch must see its
@@ -461,12 +485,14 @@ constexpr int kActRegBlocks = 4;
 template <bool F46>
 __global__ void __launch_bounds__(kActThreads)
     k_act(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
-          uint8_t* __restrict__ scales, float* __restrict__ token_scale, int* __restrict__ status) {
+          uint8_t* __restrict__ scales, float* __restrict__ token_scale, int* __restrict__ status,
+          int tiled) {
   __shared__ ScaleEnt tbl[128];
   __shared__ uint32_t red[kActThreads / 32];
   build_scale_table(tbl);
   __syncthreads();
   const int nb = H / 16;
+  const int ct = (nb + 3) / 4;  // tiled layout: tiles per tile row
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float six_m = F46 ? 1536.0f : 2688.0f;
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
@@ -517,7 +543,7 @@ __global__ void __launch_bounds__(kActThreads)
         uint32_t c0w, c1w, sb;
         quant_row_block_amax<F46>(wr[k], amax_of(bm[k]), E, tbl, c0w, c1w, sb);
         *reinterpret_cast<uint2*>(codes + row * (H / 2) + b * 8) = make_uint2(c0w, c1w);
-        scales[row * nb + b] = (uint8_t)sb;
+        scales[tiled ? scale_off_tiled(row, b, ct) : row * nb + b] = (uint8_t)sb;
       }
     }
     for (int b = threadIdx.x + kActRegBlocks * kActThreads; b < nb; b += kActThreads) {
@@ -527,21 +553,23 @@ __global__ void __launch_bounds__(kActThreads)
       uint32_t c0w, c1w, sb;
       quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
       *reinterpret_cast<uint2*>(codes + row * (H / 2) + b * 8) = make_uint2(c0w, c1w);
-      scales[row * nb + b] = (uint8_t)sb;
+      scales[tiled ? scale_off_tiled(row, b, ct) : row * nb + b] = (uint8_t)sb;
     }
     __syncthreads();
   }
 }
 
 cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* codes,
-                       uint8_t* scales, float* token_scale, int* status, cudaStream_t s) {
+                       uint8_t* scales, float* token_scale, int* status, bool tiled,
+                       cudaStream_t s) {
   if (T == 0 || H == 0) return cudaSuccess;
   const DevInfo* di = device_info();
   const int grid = (int)std::min<int64_t>(T, (int64_t)di->sms * 16);
+  const int t = tiled ? 1 : 0;
   if (f46)
-    k_act<true><<<grid, kActThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status);
+    k_act<true><<<grid, kActThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
   else
-    k_act<false><<<grid, kActThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status);
+    k_act<false><<<grid, kActThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
   return cudaGetLastError();
 }
 

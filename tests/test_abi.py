@@ -133,6 +133,15 @@ def test_validation_before_any_device_work(nvq):
     assert L.nf4_routed_linear(ok16, cntp, 2, 256, 256, _vp(FAKE + 16), ok16, ok16, P, P) == 2  # codes % 32
     assert L.nf4_routed_linear(P, C.cast(zero, C.c_void_p), 2, 256, 256, P, P, P, P, P) == 0
     assert L.nvfp4_dgrad(P, cntp, 2, 0, 256, P, P, P, P, P, P) == 1   # out == 0 still needs dX
+    L.nvq_scale_bytes.restype = C.c_int64
+    L.nvq_scale_bytes.argtypes = [C.c_int64, C.c_int64, C.c_uint]
+    assert L.nvq_scale_bytes(200, 80, 0) == 1000
+    assert L.nvq_scale_bytes(200, 80, 4) == 256 * 8
+    assert L.nvq_scale_bytes(4096, 6144, 4) == 4096 * 384
+    assert L.nvq_scale_bytes(200, 72, 4) == -1 and L.nvq_scale_bytes(-1, 16, 0) == -1
+    assert L.nvq_scale_bytes(16, 16, 8) == -1
+    assert L.nvfp4_quantize(ok16, 1, 16, 16, 8, ok16, ok16, ok16, ok16, P, P) == 4
+    assert L.act_quantize_per_token(ok16, 4, 16, 2, ok16, ok16, ok16, P, P) == 4   # amax-given: rowwise only
     assert L.nvq_debug_wait_timeout(0, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(16, P, P) == 1
