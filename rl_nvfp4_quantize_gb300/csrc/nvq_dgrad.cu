@@ -11,9 +11,10 @@
 // B is the weight slice itself, W_e [out][in] = [K][N]: N-contiguous, so the
 // producers write it MN-major, in the orientation it is stored in -- no
 // transposition.  The codes and scales of each K step (64 rows x 256 columns)
-// are staged in shared memory by TMA; producer warp w forms K rows 8w .. 8w+7
-// of the step, lane l the eight N values 8l .. 8l+7 (one code word, half a
-// scale block), so a warp reads one contiguous 128-byte row of codes.
+// are staged in shared memory by TMA; producer warp w (of 16) forms K rows
+// 4w .. 4w+3 of the step, lane l the eight N values 8l .. 8l+7 (one code
+// word, half a scale block), so a warp reads one contiguous 128-byte row of
+// codes.
 #include <cuda.h>
 #include <cstdint>
 
@@ -38,10 +39,11 @@ struct Nvfp4DgradProducer {
   static constexpr bool kMnMajor = true;
 
   float2 G2;
-  int coff;   // this lane's code word in K row 8w of a staged step
+  int coff;   // this lane's code word in K row 4w of a staged step
   int soff;   // its scale byte
-  int toff;   // its 16-byte chunk in K row 8w of the slice (unswizzled)
+  int toff;   // its 16-byte chunk in K row 4w of the slice (unswizzled)
   int chunk;  // that chunk's index within the 128-byte row
+  int phase;  // swizzle phase of K row 4w (4w & 7)
 
   __device__ static void build_extra(unsigned char*) {}
 
@@ -58,11 +60,12 @@ struct Nvfp4DgradProducer {
     const int w = p >> 5, l = p & 31;
     const float g = P.G[e];
     G2 = make_float2(g, g);
-    coff = 8 * w * 128 + 4 * l;
-    soff = kGK * 128 + 8 * w * 16 + (l >> 1);
-    // block of 64 N values l >> 3 (8 KiB apart), K row 8w
-    toff = (l >> 3) * (kGB / 4) + 8 * w * 128;
+    coff = 4 * w * 128 + 4 * l;
+    soff = kGK * 128 + 4 * w * 16 + (l >> 1);
+    // block of 64 N values l >> 3 (8 KiB apart), K row 4w
+    toff = (l >> 3) * (kGB / 4) + 4 * w * 128;
     chunk = l & 7;
+    phase = (4 * w) & 7;
   }
 
   // One code word: the eight values 8l .. 8l+7 of one K row, as four bf16
@@ -75,13 +78,14 @@ struct Nvfp4DgradProducer {
 
   __device__ __forceinline__ void produce(int, const unsigned char* cst, const unsigned char*,
                                           unsigned char* tile) const {
-    // K row 8w + i: code word at row * 128, scale byte at row * 16; in the
-    // slice it sits at (8w + i) * 128 in its block, swizzle phase i
+    // K row 4w + i: code word at row * 128, scale byte at row * 16; in the
+    // slice it sits at (4w + i) * 128 in its block, swizzle phase
+    // (4w + i) & 7 = phase + i
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
+    for (int i = 0; i < 4; i++) {
       const uint32_t c = *reinterpret_cast<const uint32_t*>(cst + coff + i * 128);
       const uint32_t S2 = e4m3_to_f16x2(cst[soff + i * 16] & 0x7f);
-      *reinterpret_cast<uint4*>(tile + toff + i * 128 + ((chunk ^ i) << 4)) =
+      *reinterpret_cast<uint4*>(tile + toff + i * 128 + ((chunk ^ (phase + i)) << 4)) =
           make_uint4(pair<0>(c, S2), pair<1>(c, S2), pair<2>(c, S2), pair<3>(c, S2));
     }
   }

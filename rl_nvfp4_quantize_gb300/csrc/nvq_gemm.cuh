@@ -10,17 +10,18 @@
 //   Y  [T][N], FP32 or bf16 (round to nearest even of the FP32 sum)
 //
 // Tile: 256 token rows (two M = 128 halves) x 256 columns of N, K in steps of
-// 64; the B slice of a K step serves both halves.  One CTA per tile, ten
+// 64; the B slice of a K step serves both halves.  One CTA per tile, 18
 // warps:
-//   warps 0-7 : producers -- form the 256 x 64 B slice of each K step in one
+//   warps 0-15: producers -- form the 256 x 64 B slice of each K step in one
 //               of SB shared stages from the packed weight data of that step
 //               (codes and scales, staged by TMA in one of SC shared stages);
-//               afterwards the epilogue (warps 0-3: token rows 0-127, warps
-//               4-7: rows 128-255): tensor memory -> registers -> Y rows;
-//   warp 8    : lane 0: TMA loads of the two X tiles [128 rows][64 K]
+//               afterwards the epilogue: tensor memory -> registers -> Y rows
+//               (warp w: accumulator rows 32 (w & 3) .. +31 of half
+//               (w >> 2) & 1, columns 128 (w >> 3) .. +127);
+//   warp 16   : lane 0: TMA loads of the two X tiles [128 rows][64 K]
 //               (128-byte swizzle) into one of SA shared stages; lane 1: TMA
 //               loads of the packed weight data of each K step;
-//   warp 9    : allocates all 512 columns of tensor memory (two 128 x 256
+//   warp 17   : allocates all 512 columns of tensor memory (two 128 x 256
 //               FP32 accumulators), issues tcgen05.mma (M 128, N 256, K 16,
 //               bf16 x bf16 -> FP32) -- four per K step and half, the second
 //               half only when the expert has rows there -- commits them to
@@ -46,8 +47,10 @@ constexpr int kGM = 128, kGN = 256, kGK = 64;
 constexpr int kGHalves = 2;                    // M halves per CTA tile
 constexpr int kGA = kGHalves * kGM * kGK * 2;  // 32 KiB of X per stage (two 16 KiB halves)
 constexpr int kGB = kGN * kGK * 2;             // 32 KiB of B per stage
-constexpr int kGThreads = 320;
-constexpr int kGProducers = 256;
+constexpr int kGProducerWarps = 16;
+constexpr int kGProducers = kGProducerWarps * 32;
+constexpr int kGTmaWarp = kGProducerWarps, kGMmaWarp = kGProducerWarps + 1;
+constexpr int kGThreads = kGProducers + 64;
 constexpr uint32_t kGTmemCols = 512;           // two FP32 accumulators of 128 x 256
 constexpr uint32_t kGWaitTries = 1u << 22;
 
@@ -155,14 +158,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
     mbar_init(acc_bar, 1);
     fence_barrier_init();
   }
-  if (warp == 9) tmem_alloc(tmem_slot, kGTmemCols);
+  if (warp == kGMmaWarp) tmem_alloc(tmem_slot, kGTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   bool ok = true;
-  if (warp < 8) {
+  if (warp < kGProducerWarps) {
     // ---- B producers
     P prod;
     prod.setup(A.w, e, n0, A.K, A.N, threadIdx.x, extra);
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         mbar_arrive(&empty_c[c]);  // the staged data of step ks has been read
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == kGTmaWarp) {
     if (lane == 0) {
       // ---- X tiles by TMA
       int issued = 0;
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           mbar_wait(&full_c[ks % SC], (ks / SC) & 1, kGWaitTries);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kGMmaWarp) {
     // ---- tensor-core issue
     if (lane == 0) {
       for (int ks = 0; ks < nk; ks++) {
@@ -250,10 +253,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
   }
 
-  // ---- epilogue: warp w reads lanes 32 (w & 3) .. +31 of accumulator w >> 2
+  // ---- epilogue
   __syncwarp();
-  if (warp < 8) {
-    const int half = warp >> 2, q = warp & 3;
+  if (warp < kGProducerWarps) {
+    // warp w reads lanes 32 (w & 3) .. +31 of accumulator (w >> 2) & 1,
+    // columns 128 (w >> 3) .. +127
+    const int q = warp & 3, half = (warp >> 2) & 1, part = warp >> 3;
     // tcgen05.ld is executed by whole warps, so the warp agrees on the wait
     if (!__all_sync(0xffffffffu, mbar_wait(acc_bar, 0, kGWaitTries))) {
       ok = false;
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const int row = tok0 + half * kGM + q * 32 + lane;
       const bool store = ok && row < tok_end;
 #pragma unroll 1
-      for (int c = 0; c < kGN / 32; c++) {
+      for (int c = part * 4; c < part * 4 + 4; c++) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * kGN + c * 32, v);
         if (store) {
@@ -286,14 +291,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
       }
     }
-  } else if (warp == 9 && lane == 0) {
+  } else if (warp == kGMmaWarp && lane == 0) {
     // the tensor memory is released only after every issued MMA has finished
     if (!mbar_wait(acc_bar, 0, kGWaitTries)) ok = false;
   }
   if (!ok && A.status) atomicOr(A.status, kStatusTimeout);
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kGMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kGTmemCols);

@@ -11,8 +11,9 @@
 //
 // B is W_e [out][in] = [N][K]: K-contiguous, one absmax per 64 K values, so one
 // NF4 block is exactly one row of a K step.  The codes (and absmax) of each K
-// step are staged in shared memory by TMA; producer thread p forms row p of
-// the slice from its 32 code bytes and its absmax.  The dequantised value of
+// step are staged in shared memory by TMA; producer thread p (of 512) forms
+// half p >> 8 of row p & 255 of the slice from 16 of its code bytes and its
+// absmax.  The dequantised value of
 // each code is bf16(level[c] * absmax), the same value nf4_dequant writes; a
 // 256-entry table maps a code byte to its two levels.
 #include <cuda.h>
@@ -44,6 +45,7 @@ struct Nf4LinearProducer {
 
   const float2* tbl;
   int p;     // this thread's row of the slice
+  int h;     // its half of the row: K values 32 h .. 32 h + 31
   int roff;  // byte offset of that row in the slice
   int phase; // its swizzle phase (row & 7)
 
@@ -66,8 +68,9 @@ struct Nf4LinearProducer {
 
   __device__ __forceinline__ void setup(const Params&, int, int, int, int, int pp,
                                         const unsigned char* extra) {
-    p = pp;
-    tbl = reinterpret_cast<const float2*>(extra) + (p & 15);
+    p = pp & (kGN - 1);
+    h = pp >> 8;
+    tbl = reinterpret_cast<const float2*>(extra) + (pp & 15);
     roff = p * 128;
     phase = p & 7;
   }
@@ -79,21 +82,20 @@ struct Nf4LinearProducer {
 
   __device__ __forceinline__ void produce(int ks, const unsigned char* cst,
                                           const unsigned char* cextra, unsigned char* tile) const {
-    // row p's 32 code bytes: two 16-byte chunks, swapped on rows with bit 2
-    // set (the 32-byte swizzle); its absmax: value ks & 3 of its 16-byte row
-    const int sw = (p >> 2) & 1;
-    const uint4 lo = *reinterpret_cast<const uint4*>(cst + p * 32 + (sw << 4));
-    const uint4 hi = *reinterpret_cast<const uint4*>(cst + p * 32 + ((sw ^ 1) << 4));
+    // half h of row p's 32 code bytes: 16-byte chunk h, swapped with the
+    // other one on rows with bit 2 set (the 32-byte swizzle); the absmax:
+    // value ks & 3 of the row's 16 bytes
+    const uint4 cv = *reinterpret_cast<const uint4*>(cst + p * 32 + ((h ^ ((p >> 2) & 1)) << 4));
     const float a = reinterpret_cast<const float*>(cextra + ((ks >> 2) & 1) * (kGN * 16))[p * 4 + (ks & 3)];
     const float2 a2 = make_float2(a, a);
-    const uint32_t cw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    // word c holds the codes of K values 8c .. 8c+7 (code 2b in the low
-    // nibble of byte b): one 16-byte chunk of the row, swizzled by phase
+    const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+    // word j holds the codes of K values 32 h + 8 j .. +7 (code 2b in the
+    // low nibble of byte b): 16-byte chunk 4 h + j of the row, swizzled by phase
 #pragma unroll
-    for (int c = 0; c < 8; c++)
-      *reinterpret_cast<uint4*>(tile + roff + ((c ^ phase) << 4)) =
-          make_uint4(pair(cw[c] & 0xffu, a2), pair((cw[c] >> 8) & 0xffu, a2),
-                     pair((cw[c] >> 16) & 0xffu, a2), pair(cw[c] >> 24, a2));
+    for (int j = 0; j < 4; j++)
+      *reinterpret_cast<uint4*>(tile + roff + (((4 * h + j) ^ phase) << 4)) =
+          make_uint4(pair(cw[j] & 0xffu, a2), pair((cw[j] >> 8) & 0xffu, a2),
+                     pair((cw[j] >> 16) & 0xffu, a2), pair(cw[j] >> 24, a2));
   }
 };
 
