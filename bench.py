@@ -604,7 +604,55 @@ def measure_context(wl, dev, peak):
     out["nvfp4_dgrad"] = measure_dgrad(stacks, wl.topk, dev)
     out["nf4_routed_linear"] = measure_nf4_linear(
         {"gate_up": (wl.nf4["codes"], wl.nf4["absmax"], GATE_UP)}, wl.topk, dev)
+    out["swizzled_scales"] = measure_swizzled(wl, dev, peak)
     return out
+
+
+def measure_swizzled(wl, dev, peak):
+    """Block scales in the tensor-core tiled layout: the dual quantisation of
+    the 32-expert gate_up stack and the per-token quantisation of the
+    [16384, 6144] activations with tiled scales (against the same calls with
+    linear scales), and the NVFP4 GEMM of cuBLASLt (torch._scaled_mm) fed
+    those outputs directly -- X [16384, 6144] x W_0^T, W_0 = [4096, 6144] --
+    as context for the layout's consumer (a library GEMM, not this
+    library's kernel)."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    res = {}
+    E, R, K = min(32, GATE_UP[0]), GATE_UP[1], GATE_UP[2]
+    n = E * R * K
+    w = wl.gu[:E]
+    lin = {k: v[:E] for k, v in wl.q_gu.items()}
+    sw = nvq.nvfp4_quantize_dual(w, four_over_six=True, swizzled_scales=True)
+    for name, o, flag in (("dual_linear", lin, False), ("dual_swizzled", sw, True)):
+        ms = cuda_timed(lambda: nvq.nvfp4_quantize_dual(w, four_over_six=True, out=o,
+                                                        swizzled_scales=flag), 5)
+        gbs = (2 * n + 2 * nvfp4_bytes(n) + 8 * E) / (ms / 1e3) / 1e9
+        res[name + "_%dx%dx%d" % (E, R, K)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                                "frac": round(gbs / peak, 4)}
+    T, H = ACTS[0]
+    x = wl.x[0]
+    qx = nvq.act_quantize_per_token(x, four_over_six=True, swizzled_scales=True)
+    ms = cuda_timed(lambda: nvq.act_quantize_per_token(x, four_over_six=True, out=qx,
+                                                       swizzled_scales=True), 10)
+    gbs = (2 * T * H + nvfp4_bytes(T * H) + 4 * T) / (ms / 1e3) / 1e9
+    res["act_swizzled_%dx%d" % (T, H)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                          "frac": round(gbs / peak, 4)}
+    if hasattr(torch, "float4_e2m1fn_x2") and H == K:
+        fp4, fp8 = torch.float4_e2m1fn_x2, torch.float8_e4m3fn
+        a, sa = qx["codes"].view(fp4), qx["scales"].view(fp8)
+        b, sb = sw["codes_row"][0].view(fp4).t(), sw["scales_row"][0].view(fp8)
+        try:
+            ms = cuda_timed(lambda: torch._scaled_mm(a, b, sa, sb, out_dtype=torch.bfloat16), 10)
+            res["cublas_nvfp4_gemm_%dx%dx%d" % (T, R, K)] = {
+                "ms": round(ms, 4), "TFLOP/s": round(2.0 * T * R * K / (ms / 1e3) / 1e12, 1),
+                "note": "cuBLASLt block-scaled FP4 GEMM reading this library's codes and tiled "
+                        "scales as produced (nominal dense FP4 peak 13500 TFLOP/s)"}
+        except (RuntimeError, TypeError) as e:
+            res["cublas_nvfp4_gemm"] = {"unavailable": str(e).splitlines()[0][:200]}
+    del sw, qx
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_dgrad(stacks, topk, dev, unfused=True):

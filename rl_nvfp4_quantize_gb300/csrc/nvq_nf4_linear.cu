@@ -48,6 +48,7 @@ struct Nf4LinearProducer {
   int h;     // its half of the row: K values 32 h .. 32 h + 31
   int roff;  // byte offset of that row in the slice
   int phase; // its swizzle phase (row & 7)
+  float4 am; // the row's absmax for the four K steps of the current slot
 
   __device__ static void build_extra(unsigned char* extra) {
     float2* t = reinterpret_cast<float2*>(extra);
@@ -81,12 +82,17 @@ struct Nf4LinearProducer {
   }
 
   __device__ __forceinline__ void produce(int ks, const unsigned char* cst,
-                                          const unsigned char* cextra, unsigned char* tile) const {
+                                          const unsigned char* cextra, unsigned char* tile) {
     // half h of row p's 32 code bytes: 16-byte chunk h, swapped with the
-    // other one on rows with bit 2 set (the 32-byte swizzle); the absmax:
-    // value ks & 3 of the row's 16 bytes
+    // other one on rows with bit 2 set (the 32-byte swizzle)
     const uint4 cv = *reinterpret_cast<const uint4*>(cst + p * 32 + ((h ^ ((p >> 2) & 1)) << 4));
-    const float a = reinterpret_cast<const float*>(cextra + ((ks >> 2) & 1) * (kGN * 16))[p * 4 + (ks & 3)];
+    // the absmax of this step is value ks & 3 of the row's 16 bytes in the
+    // slot; the four are read once per slot (one 16-byte read: a warp's 32
+    // rows are contiguous, so the read is conflict-free)
+    if ((ks & 3) == 0)
+      am = *reinterpret_cast<const float4*>(cextra + ((ks >> 2) & 1) * (kGN * 16) + p * 16);
+    const int k4 = ks & 3;
+    const float a = k4 == 0 ? am.x : k4 == 1 ? am.y : k4 == 2 ? am.z : am.w;
     const float2 a2 = make_float2(a, a);
     const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
     // word j holds the codes of K values 32 h + 8 j .. +7 (code 2b in the

@@ -2,6 +2,10 @@
 times, checked on sampled outputs the oracle computes one by one.
 
 Workloads (seeded, synthetic, generated on the GPU):
+  * the dgrad GEMM through the rowwise NVFP4 copy and the NF4 forward GEMM of
+    the 256-expert gate_up stack for the 8192-token top-8 Zipf(1.1) router
+    (65536 grouped token rows), sampled rows of the largest, the smallest and
+    six other routed experts;
   * expert stack [32, 4096, 6144] and the 256-expert layer gate_up
     [256, 4096, 6144] + down [256, 6144, 2048], N(0, 0.02 u_e) with 0.05 %
     outliers x 30: dual-layout NVFP4 + Four-Over-Six, then the transposed
@@ -69,18 +73,17 @@ def _check_dual_sampled(oracle_mod, w, r, rng, four_over_six=True):
     return experts
 
 
-def _check_dequant_t_sampled(oracle_mod, r, dt, experts, rng):
-    E, R, K2 = r["codes_row"].shape
-    K = 2 * K2
+def _check_dequant_t_sampled(oracle_mod, w, dt, experts, rng):
+    """Columns of DQ(Q(w))^T against the oracle's own quantisation of the
+    same weight rows (under the expert's amax, computed by the oracle)."""
+    E, R, K = w.shape
     for e in experts:
-        rows = rng.integers(0, R, 4)
-        codes = r["codes_row"][e].cpu().numpy()
-        scales = r["scales_row"][e].cpu().numpy()
-        G = np.array([r["tensor_scale"][e].item()], np.float32)
+        xe = u16(w[e])
+        amax = np.array([oracle_mod.amax_bf16(xe)], np.float32)
         got = u16(dt[e])                                  # [K, R]
-        for i in rows:
-            ref = oracle_mod.nvfp4_dequant(codes[i:i + 1].reshape(1, 1, K2), scales[i:i + 1].reshape(1, 1, K // 16),
-                                           G, 1, K)[0, 0]
+        for i in rng.integers(0, R, 4):
+            o = oracle_mod.nvfp4_quantize(xe[i:i + 1].reshape(1, 1, K), four_over_six=True, amax=amax)
+            ref = oracle_mod.nvfp4_dequant(o["codes"], o["scales"], o["G"], 1, K)[0, 0]
             assert_same(got[:, i], ref, "dequant_t column %d of expert %d" % (i, e))
 
 
@@ -93,7 +96,7 @@ def test_dual_32_experts_sampled(nvq, oracle_mod, shape):
     torch.cuda.synchronize()
     rng = np.random.default_rng(22)
     experts = _check_dual_sampled(oracle_mod, w, r, rng)
-    _check_dequant_t_sampled(oracle_mod, r, dt, experts, rng)
+    _check_dequant_t_sampled(oracle_mod, w, dt, experts, rng)
     del w, r, dt
     torch.cuda.empty_cache()
 
@@ -109,7 +112,7 @@ def test_moe_layer_256_experts_sampled(nvq, oracle_mod):
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         experts = _check_dual_sampled(oracle_mod, w, r, rng)
-        _check_dequant_t_sampled(oracle_mod, r, dt, experts, rng)
+        _check_dequant_t_sampled(oracle_mod, w, dt, experts, rng)
         # every slice scale is consistent with its amax (all 256, exactly)
         am = r["amax"].cpu().numpy()
         G = r["tensor_scale"].cpu().numpy()
@@ -181,3 +184,79 @@ def test_nf4_routed_few_tokens_leaves_unrouted_slices(nvq, oracle_mod):
             assert torch.equal(dv[e], fv[e]), e
         else:
             assert bool((dv[e] == 0x7A7A).all()), e
+
+
+def _sample_rows(counts, rng):
+    """Token rows to check: the first and last row of the largest expert, of
+    the smallest routed one and of six others, plus two random rows of each;
+    returns (expert, rows of that expert as offsets into the grouped rows)."""
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    routed = [e for e in range(len(counts)) if counts[e] > 0]
+    pick = {int(np.argmax(counts)), min(routed, key=lambda e: counts[e])}
+    pick.update(int(e) for e in rng.choice(routed, 6, replace=False))
+    out = []
+    for e in sorted(pick):
+        r = {offs[e], offs[e + 1] - 1} | set(int(x) for x in rng.integers(offs[e], offs[e + 1], 2))
+        out.append((e, np.array(sorted(r))))
+    return out
+
+
+def test_dgrad_full_size_sampled(nvq, oracle_mod):
+    """dX = dY . DQ(Q(W_e)) for the 256-expert gate_up stack and the
+    8192-token top-8 Zipf(1.1) router (65536 grouped rows), as the benchmark
+    times it; sampled rows against the oracle, which quantises the sampled
+    experts itself.  Tolerance as in the small dgrad tests."""
+    from rl_nvfp4_quantize_gb300 import synth
+    E, R, K = 256, 4096, 6144
+    w = synth.expert_weights(E, R, K, seed=12, device="cuda")
+    q = nvq.nvfp4_quantize(w, four_over_six=True)
+    topk = synth.zipf_router(8192, E, 8, seed=13, device="cuda")
+    counts = torch.bincount(topk.flatten().long(), minlength=E).cpu().numpy()
+    T = int(counts.sum())
+    dy = synth.activations(T, R, seed=14, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dx = nvq.nvfp4_dgrad(dy, counts.tolist(), q["codes"], q["scales"], q["tensor_scale"], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(66)
+    for e, rows in _sample_rows(counts, rng):
+        o = oracle_mod.nvfp4_quantize(u16(w[e:e + 1]), four_over_six=True)
+        idx = torch.from_numpy(rows).cuda()
+        ref, bound = oracle_mod.nvfp4_dgrad(u16(dy[idx]), [len(rows)], o["codes"], o["scales"],
+                                            o["G"], R, K)
+        got = dx[idx].cpu().numpy().astype(np.float64)
+        tol = R * 2.0 ** -23 * bound + 1e-30
+        assert np.all(np.abs(got - ref) <= tol), (e, float((np.abs(got - ref) - tol).max()))
+    del w, q, dy, dx
+    torch.cuda.empty_cache()
+
+
+def test_nf4_linear_full_size_sampled(nvq, oracle_mod):
+    """Y = X . DQ(W_e)^T for the 256-expert NF4 gate_up stack and the same
+    router, as the benchmark times it; sampled rows against the oracle, which
+    quantises the sampled experts itself.  Tolerance as in the small NF4
+    forward tests."""
+    from rl_nvfp4_quantize_gb300 import synth
+    E, R, K = 256, 4096, 6144
+    w = synth.expert_weights(E, R, K, seed=15, device="cuda")
+    q = nvq.nf4_quantize(w)
+    topk = synth.zipf_router(8192, E, 8, seed=16, device="cuda")
+    counts = torch.bincount(topk.flatten().long(), minlength=E).cpu().numpy()
+    T = int(counts.sum())
+    x = synth.activations(T, K, seed=17, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = nvq.nf4_routed_linear(x, counts.tolist(), q["codes"], q["absmax"], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(77)
+    for e, rows in _sample_rows(counts, rng):
+        o = oracle_mod.nf4_quantize(u16(w[e:e + 1]))
+        idx = torch.from_numpy(rows).cuda()
+        ref, bound = oracle_mod.nf4_routed_linear(u16(x[idx]), [len(rows)], o["codes"], o["absmax"],
+                                                  R, K)
+        got = (u16(y[idx]).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        d = K * 2.0 ** -23 * bound
+        tol = 2.0 ** -8 * (np.abs(ref) + d) + d
+        assert np.all(np.abs(got - ref) <= tol), (e, float((np.abs(got - ref) - tol).max()))
+    del w, q, x, y
+    torch.cuda.empty_cache()
