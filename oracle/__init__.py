@@ -93,6 +93,14 @@ def _load():
             lib.oracle_nf4_dequant.argtypes = [P, P, i64, i64, i64, P]
             lib.oracle_routed_union.restype = None
             lib.oracle_routed_union.argtypes = [P, i64, i64, i64, P, P, P]
+            lib.oracle_mxfp8_block.restype = C.c_uint8
+            lib.oracle_mxfp8_block.argtypes = [P, i64, P]
+            for name in ("oracle_mxfp8_quantize", "oracle_mxfp8_quantize_colwise"):
+                f = getattr(lib, name)
+                f.restype = None
+                f.argtypes = [P, i64, i64, i64, P, P]
+            lib.oracle_mxfp8_dequant.restype = None
+            lib.oracle_mxfp8_dequant.argtypes = [P, P, i64, P]
             lib.oracle_nf4_dequant_routed.restype = None
             lib.oracle_nf4_dequant_routed.argtypes = [P, P, i64, i64, i64, P, i64, i64, P, P, P, P]
             _lib = lib
@@ -416,3 +424,44 @@ def nvfp4_scaled_product(a_codes, a_scales, b_codes, b_scales):
     va = nvfp4_block_values(a_codes, a_scales)
     vb = nvfp4_block_values(b_codes, b_scales)
     return va @ vb.T, np.abs(va) @ np.abs(vb).T
+
+
+def mxfp8_block(x32: np.ndarray):
+    """One MXFP8 block of 32 bf16 values: (scale byte, codes [32])."""
+    x = np.ascontiguousarray(x32, np.uint16)
+    codes = np.zeros(32, np.uint8)
+    s = _load().oracle_mxfp8_block(_p(x), 1, _p(codes))
+    return int(s), codes
+
+
+def mxfp8_quantize(w: np.ndarray):
+    """MXFP8 of w [nexp, rows, cols] with 1x32 blocks along cols (OCP MX:
+    E8M0 scale per block, E4M3 elements; "The 4-bitter Lesson", "Key
+    claims": the MXFP8 validation of the dequantised backward).  Returns
+    codes [nexp, rows, cols] and scales [nexp, rows, cols/32]."""
+    w = _u16(w)
+    nexp, rows, cols = w.shape
+    codes = np.zeros((nexp, rows, cols), np.uint8)
+    scales = np.zeros((nexp, rows, cols // 32), np.uint8)
+    _load().oracle_mxfp8_quantize(_p(w), nexp, rows, cols, _p(codes), _p(scales))
+    return dict(codes=codes, scales=scales)
+
+
+def mxfp8_quantize_colwise(w: np.ndarray):
+    """MXFP8 with 32x1 blocks along rows, stored transposed: codes
+    [nexp, cols, rows], scales [nexp, cols, rows/32]."""
+    w = _u16(w)
+    nexp, rows, cols = w.shape
+    codes = np.zeros((nexp, cols, rows), np.uint8)
+    scales = np.zeros((nexp, cols, rows // 32), np.uint8)
+    _load().oracle_mxfp8_quantize_colwise(_p(w), nexp, rows, cols, _p(codes), _p(scales))
+    return dict(codes=codes, scales=scales)
+
+
+def mxfp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """bf16 bits of E4M3 value x 2^(scale - 127), in the layout of the codes."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    dst = np.zeros(codes.shape, np.uint16)
+    _load().oracle_mxfp8_dequant(_p(codes), _p(scales), codes.size, _p(dst))
+    return dst

@@ -578,3 +578,85 @@ ORACLE_API void oracle_f32_to_bf16_n(const float* x, uint16_t* out, int64_t n)
 {
     for (int64_t i = 0; i < n; i++) out[i] = oracle_f32_to_bf16(x[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8 (row F4): the format "The 4-bitter Lesson" ("Key claims") used to   */
+/* validate the dequantised backward before NVFP4.  The pages name it only;  */
+/* its definition is the OCP Microscaling (MX) one: blocks of 32 consecutive */
+/* elements share one E8M0 scale X = 2^s, and each element is stored as the  */
+/* E4M3 value of v / X.                                                     */
+/*   s = floor(log2(amax)) - 8, 8 being the exponent of the largest power of */
+/*       two in E4M3 (256); clamped to [-127, 127]; amax = 0 gives -127;     */
+/*   scale byte = s + 127 (E8M0: the value 2^(byte - 127));                  */
+/*   element = E4M3(v * 2^-s), nearest with ties to even, saturating at 448  */
+/*       (values in (448, 512) clamp), carrying the sign of v (so -0 and     */
+/*       negative values that round to zero give 0x80).                      */
+/* v * 2^-s is exact in binary32 whenever its E4M3 value is not zero.        */
+/* ------------------------------------------------------------------------ */
+
+static int mx_shared_exp(float amax)
+{
+    if (!(amax > 0.0f)) return -127;
+    int e;
+    frexpf(amax, &e);            /* amax = m * 2^e, m in [0.5, 1): floor(log2 amax) = e - 1 */
+    int s = (e - 1) - 8;
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+static uint8_t e4m3_signed(float x)
+{
+    uint8_t m = oracle_e4m3_encode(fabsf(x));
+    return signbit(x) ? (uint8_t)(m | 0x80u) : m;
+}
+
+/* One block of 32 bf16 values x[0], x[stride], ...: the 32 codes and the
+ * returned scale byte. */
+ORACLE_API uint8_t oracle_mxfp8_block(const uint16_t* x, int64_t stride, uint8_t codes[32])
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        float a = fabsf(oracle_bf16_to_f32(x[i * stride]));
+        if (a > amax) amax = a;
+    }
+    int s = mx_shared_exp(amax);
+    float inv = ldexpf(1.0f, -s);
+    for (int i = 0; i < 32; i++) codes[i] = e4m3_signed(oracle_bf16_to_f32(x[i * stride]) * inv);
+    return (uint8_t)(s + 127);
+}
+
+/* Rowwise: blocks of 1x32 along cols.  codes [nexp, rows, cols], scales
+ * [nexp, rows, cols/32]; cols % 32 == 0. */
+ORACLE_API void oracle_mxfp8_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols,
+                                      uint8_t* codes, uint8_t* scales)
+{
+    for (int64_t e = 0; e < nexp; e++)
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t b = 0; b < cols / 32; b++) {
+                int64_t i = (e * rows + r) * cols + 32 * b;
+                scales[(e * rows + r) * (cols / 32) + b] = oracle_mxfp8_block(w + i, 1, codes + i);
+            }
+}
+
+/* Columnwise: blocks of 32x1 along rows, stored transposed (K-major for the
+ * transposed product): codes [nexp, cols, rows], scales [nexp, cols, rows/32];
+ * rows % 32 == 0. */
+ORACLE_API void oracle_mxfp8_quantize_colwise(const uint16_t* w, int64_t nexp, int64_t rows,
+                                              int64_t cols, uint8_t* codes, uint8_t* scales)
+{
+    for (int64_t e = 0; e < nexp; e++)
+        for (int64_t c = 0; c < cols; c++)
+            for (int64_t b = 0; b < rows / 32; b++) {
+                const uint16_t* x = w + (e * rows + 32 * b) * cols + c;
+                scales[(e * cols + c) * (rows / 32) + b] =
+                    oracle_mxfp8_block(x, cols, codes + (e * cols + c) * rows + 32 * b);
+            }
+}
+
+/* y = bf16(E4M3 value * 2^(byte - 127)) (the product is exact in binary32),
+ * for n elements in the layout of the codes (one scale per 32). */
+ORACLE_API void oracle_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n,
+                                     uint16_t* dst)
+{
+    for (int64_t i = 0; i < n; i++)
+        dst[i] = oracle_f32_to_bf16(ldexpf(oracle_e4m3_value(codes[i]), (int)scales[i / 32] - 127));
+}
