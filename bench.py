@@ -605,7 +605,37 @@ def measure_context(wl, dev, peak):
     out["nf4_routed_linear"] = measure_nf4_linear(
         {"gate_up": (wl.nf4["codes"], wl.nf4["absmax"], GATE_UP)}, wl.topk, dev)
     out["swizzled_scales"] = measure_swizzled(wl, dev, peak)
+    out["mxfp8"] = measure_mxfp8(wl, peak)
     return out
+
+
+def measure_mxfp8(wl, peak):
+    """MXFP8 (row F4) of the 32-expert gate_up stack [32, 4096, 6144]:
+    rowwise only (bf16 in 2 B, codes 1 B + scales 1/32 B per element) and
+    rowwise + columnwise from one read (2 + 2 x (1 + 1/32) B per element), and
+    the dequantisation of the rowwise copy (1 + 1/32 B in, 2 B out)."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    E, R, K = min(32, GATE_UP[0]), GATE_UP[1], GATE_UP[2]
+    n = E * R * K
+    w = wl.gu[:E]
+    res = {}
+    q = nvq.mxfp8_quantize(w, columnwise=True)
+    for name, col, b in (("mxfp8_quantize_rowwise", False, 2 * n + n + n // 32),
+                         ("mxfp8_quantize_dual", True, 2 * n + 2 * (n + n // 32))):
+        o = q if col else {"codes_row": q["codes_row"], "scales_row": q["scales_row"]}
+        ms = cuda_timed(lambda: nvq.mxfp8_quantize(w, columnwise=col, out=o), 5)
+        gbs = b / (ms / 1e3) / 1e9
+        res["%s_%dx%dx%d" % (name, E, R, K)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                                 "frac": round(gbs / peak, 4)}
+    d = torch.empty((E, R, K), dtype=torch.bfloat16, device=w.device)
+    ms = cuda_timed(lambda: nvq.mxfp8_dequant(q["codes_row"], q["scales_row"], out=d), 5)
+    gbs = (n + n // 32 + 2 * n) / (ms / 1e3) / 1e9
+    res["mxfp8_dequant_%dx%dx%d" % (E, R, K)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                                  "frac": round(gbs / peak, 4)}
+    del q, d
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_swizzled(wl, dev, peak):

@@ -313,6 +313,46 @@ NVQ_API int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t 
                               int* status, nvq_stream_t stream);
 
 /*
+ * mxfp8_quantize -- MXFP8 of an expert stack, rowwise and optionally
+ * columnwise from one read.  [P4] "Key claims": the dequantised backward was
+ * validated first with MXFP8.  The pages name the format only; this is the
+ * OCP Microscaling definition: blocks of 32 elements along one axis share a
+ * scale 2^s stored as an E8M0 byte s + 127, with s = floor(log2 amax) - 8
+ * clamped to [-127, 127] (amax = 0 gives -127); each element is the E4M3 value
+ * of v * 2^-s (an exact product), rounded to nearest even, saturating at 448
+ * (so the top of a binade can clamp), sign kept.  No global scale.
+ *
+ *   w           in   bf16 [nexp, rows, cols]; cols % 32 == 0
+ *   codes_row   out  u8 [nexp, rows, cols] (E4M3)   scales_row out u8 [nexp, rows, cols/32]
+ *   codes_col   out  u8 [nexp, cols, rows], nullable: the columnwise copy (32x1 blocks along
+ *                    rows, stored transposed, K-major for the transposed product);
+ *                    rows % 32 == 0 when given
+ *   scales_col  out  u8 [nexp, cols, rows/32] (null iff codes_col is)
+ *   flags       0 or NVQ_SCALES_SWIZZLED (tiled layout as for NVFP4, with 32-element
+ *               blocks; sizes from nvq_mx_scale_bytes)
+ *   status      device int, nullable: NVQ_STATUS_NONFINITE if a block amax is infinite
+ *               (NaN inputs are out of contract)
+ */
+NVQ_API int mxfp8_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols,
+                           unsigned flags, uint8_t* codes_row, uint8_t* scales_row,
+                           uint8_t* codes_col, uint8_t* scales_col, int* status,
+                           nvq_stream_t stream);
+
+/*
+ * mxfp8_dequant -- y = bf16(E4M3 value * 2^(byte - 127)) for n codes in any
+ * layout whose blocks of 32 are contiguous (either copy of mxfp8_quantize):
+ * the product is exact, the bf16 conversion rounds to nearest even.
+ *   codes in u8 [n]; scales in u8 [n/32] (linear); dst out bf16 [n]; n % 32 == 0
+ */
+NVQ_API int mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* dst,
+                          nvq_stream_t stream);
+
+/* Bytes of the MXFP8 block scales of one [rows, cols] slice (cols % 32 == 0):
+   rows * cols / 32 linearly, or the padded tiled size with
+   NVQ_SCALES_SWIZZLED.  -1 for invalid arguments.  Host only. */
+NVQ_API int64_t nvq_mx_scale_bytes(int64_t rows, int64_t cols, unsigned flags);
+
+/*
  * nvq_debug_convert -- runs one device rounding primitive elementwise, for
  * conversion sweeps against an independent implementation.
  *   kind 0: f32 -> E4M3 byte (RNE, satfinite); in f32[n], out u8[n]

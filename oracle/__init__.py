@@ -465,3 +465,11 @@ def mxfp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     dst = np.zeros(codes.shape, np.uint16)
     _load().oracle_mxfp8_dequant(_p(codes), _p(scales), codes.size, _p(dst))
     return dst
+
+
+def mxfp8_values(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """E4M3 value x 2^(scale - 127) of every element, float64 and exact;
+    codes [..., K] with linear scales [..., K/32]."""
+    e4 = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    sc = np.ldexp(1.0, np.asarray(scales, np.int64) - 127)
+    return e4[np.asarray(codes, np.uint8)] * np.repeat(sc, 32, axis=-1)

@@ -25,6 +25,7 @@ __all__ = [
     "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "FLAG_SCALES_SWIZZLED", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
     "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t", "nvfp4_dgrad",
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed", "nf4_routed_linear",
+    "mxfp8_quantize", "mxfp8_dequant", "mx_scale_bytes",
     "nf4_codebook", "scale_bytes", "debug_convert", "debug_wait_timeout", "lib", "library_path",
 ]
 
@@ -69,6 +70,9 @@ def _load():
         "nvq_debug_wait_timeout": ([u32, P, P], i32),
         "nvfp4_dgrad": ([P, P, i64, i64, i64, P, P, P, P, P, P], i32),
         "nf4_routed_linear": ([P, P, i64, i64, i64, P, P, P, P, P], i32),
+        "mxfp8_quantize": ([P, i64, i64, i64, u32, P, P, P, P, P, P], i32),
+        "mxfp8_dequant": ([P, P, i64, P, P], i32),
+        "nvq_mx_scale_bytes": ([i64, i64, u32], i64),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -320,4 +324,53 @@ def nf4_routed_linear(x, counts, codes, absmax, status=None, stream=None, out=No
     _check("nf4_routed_linear", lib.nf4_routed_linear(_ptr(_bf16(x, "x")), C.cast(cnt, C.c_void_p),
                                                       E, R, K, _ptr(codes), _ptr(absmax), _ptr(dst),
                                                       _ptr(status), _stream(stream)))
+    return dst
+
+
+# ---------------------------------------------------------------- MXFP8
+
+def mx_scale_bytes(rows, cols, swizzled=False):
+    """Bytes of the MXFP8 block scales of one [rows, cols] slice (see
+    nvq_mx_scale_bytes in nvq.h)."""
+    n = lib.nvq_mx_scale_bytes(rows, cols, FLAG_SCALES_SWIZZLED if swizzled else 0)
+    if n < 0:
+        raise ValueError("invalid MXFP8 scale shape [%d, %d]" % (rows, cols))
+    return n
+
+
+def mxfp8_quantize(w, columnwise=False, swizzled_scales=False, status=None, stream=None, out=None):
+    """MXFP8 of w [nexp, rows, cols] (bf16): codes_row [nexp, rows, cols] u8
+    (E4M3), scales_row [nexp, rows, cols/32] u8 (E8M0) and, with columnwise,
+    codes_col [nexp, cols, rows] / scales_col [nexp, cols, rows/32] from the
+    same read.  With swizzled_scales the scales are [nexp, bytes] in the
+    tensor-core tiled layout."""
+    w = _as3d(_bf16(w, "w"))
+    E, R, K = w.shape
+    o = out or {}
+
+    def sc(rows, cols):
+        if swizzled_scales:
+            return _empty((E, mx_scale_bytes(rows, cols, True)), torch.uint8, w)
+        return _empty((E, rows, cols // 32), torch.uint8, w)
+    cr = o.get("codes_row", _empty((E, R, K), torch.uint8, w))
+    sr = o.get("scales_row") if "scales_row" in o else sc(R, K)
+    cc = sco = None
+    if columnwise:
+        cc = o.get("codes_col", _empty((E, K, R), torch.uint8, w))
+        sco = o.get("scales_col") if "scales_col" in o else sc(K, R)
+    flags = FLAG_SCALES_SWIZZLED if swizzled_scales else 0
+    _check("mxfp8_quantize", lib.mxfp8_quantize(_ptr(w), E, R, K, flags, _ptr(cr), _ptr(sr), _ptr(cc),
+                                                _ptr(sco), _ptr(status), _stream(stream)))
+    r = dict(codes_row=cr, scales_row=sr)
+    if columnwise:
+        r.update(codes_col=cc, scales_col=sco)
+    return r
+
+
+def mxfp8_dequant(codes, scales, stream=None, out=None):
+    """bf16 of MXFP8 codes (any shape whose last dimension holds whole blocks
+    of 32) with their linear scales."""
+    dst = out if out is not None else _empty(tuple(codes.shape), torch.bfloat16, codes)
+    _check("mxfp8_dequant", lib.mxfp8_dequant(_ptr(codes), _ptr(scales), codes.numel(), _ptr(dst),
+                                              _stream(stream)))
     return dst

@@ -491,6 +491,57 @@ int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t nexp, in
                                               y, status, cs(stream)));
 }
 
+int64_t nvq_mx_scale_bytes(int64_t rows, int64_t cols, unsigned flags) {
+  if (rows < 0 || cols < 0 || cols % 32 || (flags & ~(unsigned)NVQ_SCALES_SWIZZLED)) return -1;
+  if (rows > (1ll << 40) || cols > (1ll << 40)) return -1;
+  return (flags & NVQ_SCALES_SWIZZLED) ? nvq::tiled_bytes(rows, cols / 32) : rows * (cols / 32);
+}
+
+int mxfp8_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, unsigned flags,
+                   uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
+                   int* status, nvq_stream_t stream) {
+  if (flags & ~(unsigned)NVQ_SCALES_SWIZZLED) return NVQ_ERR_FLAGS;
+  int64_t total;
+  int rc = check_stack(nexp, rows, cols, &total);
+  if (rc) return rc;
+  const bool dual = codes_col != nullptr || scales_col != nullptr;
+  if (cols % 32 || (dual && rows % 32)) return NVQ_ERR_SHAPE;
+  if (total == 0) return NVQ_OK;
+  if (!w || !codes_row || !scales_row || (dual && (!codes_col || !scales_col))) return NVQ_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(codes_row, 16) || !aligned(scales_row, 16) ||
+      (dual && (!aligned(codes_col, 16) || !aligned(scales_col, 16))) ||
+      (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  if ((rc = device_check())) return rc;
+  cudaStream_t s = cs(stream);
+  const bool tiled = flags & NVQ_SCALES_SWIZZLED;
+  if (tiled) {
+    // the kernel writes only the real entries of the padded tiled layout
+    if ((rows % 128 || (cols / 32) % 4) &&
+        (rc = launch_result(cudaMemsetAsync(
+             scales_row, 0, (size_t)(nexp * nvq::tiled_bytes(rows, cols / 32)), s))))
+      return rc;
+    if (dual && (cols % 128 || (rows / 32) % 4) &&
+        (rc = launch_result(cudaMemsetAsync(
+             scales_col, 0, (size_t)(nexp * nvq::tiled_bytes(cols, rows / 32)), s))))
+      return rc;
+  }
+  return launch_result(nvq::launch_mx_tiles(w, nexp, (int)rows, (int)cols, codes_row, scales_row,
+                                            dual ? codes_col : nullptr, scales_col, status, tiled,
+                                            s));
+}
+
+int mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* dst,
+                  nvq_stream_t stream) {
+  if (n < 0 || n % 32 || n >= (1ll << 46)) return NVQ_ERR_SHAPE;
+  if (n == 0) return NVQ_OK;
+  if (!codes || !scales || !dst) return NVQ_ERR_NULL;
+  if (!aligned(codes, 16) || !aligned(dst, 16)) return NVQ_ERR_ALIGN;
+  int rc = device_check();
+  if (rc) return rc;
+  return launch_result(nvq::launch_mx_dequant(codes, scales, n, dst, cs(stream)));
+}
+
 int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream) {
   if (max_tries == 0 || max_tries > 65536u) return NVQ_ERR_SHAPE;
   if (!status) return NVQ_ERR_NULL;

@@ -54,12 +54,13 @@ cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, floa
 // With compute_amax the per-slice amax (zeroed by the caller) is reduced
 // here: the first chunk of slices by a reduction pass, every later chunk
 // inside the launch that quantises the chunk before it.
-// Bytes of the block scales of one [rows, cols] slice in the tensor-core
-// tiled layout: rows padded to a multiple of 128, blocks per row (cols / 16)
-// to a multiple of 4.
-inline int64_t tiled_scale_bytes(int64_t rows, int64_t cols) {
-  return (rows + 127) / 128 * 128 * ((cols / 16 + 3) / 4 * 4);
+// Bytes of a [rows, nblocks] matrix of block scales in the tensor-core tiled
+// layout: rows padded to a multiple of 128, blocks per row to a multiple of 4.
+inline int64_t tiled_bytes(int64_t rows, int64_t nblocks) {
+  return (rows + 127) / 128 * 128 * ((nblocks + 3) / 4 * 4);
 }
+// The same for the NVFP4 scales of a [rows, cols] slice (16-element blocks).
+inline int64_t tiled_scale_bytes(int64_t rows, int64_t cols) { return tiled_bytes(rows, cols / 16); }
 
 // With tiled, the block scales are written in the tensor-core tiled layout
 // (padding entries are the caller's to zero).
@@ -90,6 +91,15 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const float* absmax, int64_
 
 cudaError_t launch_routed_union(const int32_t* topk, int64_t n_idx, int nexp, int32_t* hit_list,
                                 int32_t* n_hit, int* status, cudaStream_t s);
+
+// MXFP8 of a stack: rowwise (1x32 blocks) and, with codes_col != nullptr,
+// columnwise (32x1 blocks, stored transposed) from one read.
+cudaError_t launch_mx_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, uint8_t* codes_row,
+                            uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
+                            int* status, bool tiled, cudaStream_t s);
+// bf16 of n MXFP8 codes (n % 32 == 0) with one scale byte per 32.
+cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* dst,
+                              cudaStream_t s);
 
 cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n, cudaStream_t s);
 cudaError_t launch_debug_wait_timeout(uint32_t max_tries, int* status, cudaStream_t s);

@@ -142,6 +142,22 @@ def test_validation_before_any_device_work(nvq):
     assert L.nvq_scale_bytes(16, 16, 8) == -1
     assert L.nvfp4_quantize(ok16, 1, 16, 16, 8, ok16, ok16, ok16, ok16, P, P) == 4
     assert L.act_quantize_per_token(ok16, 4, 16, 2, ok16, ok16, ok16, P, P) == 4   # amax-given: rowwise only
+    L.nvq_mx_scale_bytes.restype = C.c_int64
+    L.nvq_mx_scale_bytes.argtypes = [C.c_int64, C.c_int64, C.c_uint]
+    assert L.nvq_mx_scale_bytes(200, 160, 0) == 1000
+    assert L.nvq_mx_scale_bytes(200, 160, 4) == 256 * 8
+    assert L.nvq_mx_scale_bytes(200, 48, 0) == -1
+    assert L.mxfp8_quantize(ok16, 1, 32, 48, 0, ok16, ok16, P, P, P, P) == 3        # cols % 32
+    assert L.mxfp8_quantize(ok16, 1, 48, 64, 0, ok16, ok16, ok16, ok16, P, P) == 3  # rows % 32 (dual)
+    assert L.mxfp8_quantize(ok16, 1, 48, 64, 0, ok16, ok16, P, P, P, P) == 5 or \
+        L.mxfp8_quantize(ok16, 1, 48, 64, 0, ok16, ok16, P, P, P, P) == 0          # rowwise: any rows
+    assert L.mxfp8_quantize(ok16, 1, 32, 64, 8, ok16, ok16, P, P, P, P) == 4        # unknown flag
+    assert L.mxfp8_quantize(ok16, 1, 32, 64, 0, ok16, ok16, ok16, P, P, P) == 1     # half a column copy
+    assert L.mxfp8_quantize(mis, 1, 32, 64, 0, ok16, ok16, P, P, P, P) == 2
+    assert L.mxfp8_quantize(P, 0, 32, 64, 0, P, P, P, P, P, P) == 0
+    assert L.mxfp8_dequant(ok16, ok16, 48, ok16, P) == 3
+    assert L.mxfp8_dequant(ok16, P, 64, ok16, P) == 1
+    assert L.mxfp8_dequant(P, P, 0, P, P) == 0
     assert L.nvq_debug_wait_timeout(0, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(16, P, P) == 1
