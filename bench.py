@@ -368,7 +368,7 @@ def main():
                     help="skip the context measurements outside the step")
     ap.add_argument("--unfused", action="store_true",
                     help="with --case: also time the dequant + per-expert cuBLAS comparison")
-    ap.add_argument("--case", default=None, choices=["dgrad", "nf4_linear"],
+    ap.add_argument("--case", default=None, choices=["dgrad", "nf4_linear", "mxfp8"],
                     help="run one context measurement alone on a reduced case (profiling)")
     ap.add_argument("--tokens", type=int, default=2048,
                     help="router tokens of --case")
@@ -784,14 +784,23 @@ def run_case(args):
     and down stacks of --experts slices rowwise (NVFP4, Four-Over-Six),
     --case nf4_linear quantises them to NF4; both route --tokens tokens top-8
     with the Zipf(1.1) router and time nvfp4_dgrad / nf4_routed_linear on
-    both stacks (the cuBLAS comparison only with --unfused).  Prints one JSON
-    object."""
+    both stacks (the cuBLAS comparison only with --unfused).  --case mxfp8
+    times the MXFP8 calls on a gate_up stack of --experts slices.  Prints one
+    JSON object."""
     import torch
     import rl_nvfp4_quantize_gb300 as nvq
     from rl_nvfp4_quantize_gb300 import synth
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     E = GATE_UP[0]
+    if args.case == "mxfp8":
+        class _W:  # the stack measure_mxfp8 reads, without the rest of the workload
+            pass
+        wl = _W()
+        wl.gu = synth.expert_weights(*GATE_UP, seed=2, device=dev)
+        peak, _ = load_peaks()
+        print(json.dumps({"case": args.case, "experts": E, "result": measure_mxfp8(wl, peak)}))
+        return
     stacks = {}
     for name, shape, seed in (("gate_up", GATE_UP, 2), ("down", DOWN, 3)):
         w = synth.expert_weights(*shape, seed=seed, device=dev)

@@ -323,8 +323,9 @@ NVQ_API int nf4_routed_linear(const uint16_t* x, const int64_t* counts, int64_t 
  * (so the top of a binade can clamp), sign kept.  No global scale.
  *
  *   w           in   bf16 [nexp, rows, cols]; cols % 32 == 0
- *   codes_row   out  u8 [nexp, rows, cols] (E4M3)   scales_row out u8 [nexp, rows, cols/32]
- *   codes_col   out  u8 [nexp, cols, rows], nullable: the columnwise copy (32x1 blocks along
+ *   codes_row   out  u8 [nexp, rows, cols] (E4M3, 32-byte aligned)
+ *   scales_row  out  u8 [nexp, rows, cols/32]
+ *   codes_col   out  u8 [nexp, cols, rows] (32-byte aligned), nullable: the columnwise copy (32x1 blocks along
  *                    rows, stored transposed, K-major for the transposed product);
  *                    rows % 32 == 0 when given
  *   scales_col  out  u8 [nexp, cols, rows/32] (null iff codes_col is)
@@ -342,7 +343,8 @@ NVQ_API int mxfp8_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_
  * mxfp8_dequant -- y = bf16(E4M3 value * 2^(byte - 127)) for n codes in any
  * layout whose blocks of 32 are contiguous (either copy of mxfp8_quantize):
  * the product is exact, the bf16 conversion rounds to nearest even.
- *   codes in u8 [n]; scales in u8 [n/32] (linear); dst out bf16 [n]; n % 32 == 0
+ *   codes in u8 [n]; scales in u8 [n/32] (linear); dst out bf16 [n] (32-byte
+ *   aligned); n % 32 == 0
  */
 NVQ_API int mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* dst,
                           nvq_stream_t stream);

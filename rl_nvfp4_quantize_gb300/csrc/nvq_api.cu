@@ -508,8 +508,8 @@ int mxfp8_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, 
   if (cols % 32 || (dual && rows % 32)) return NVQ_ERR_SHAPE;
   if (total == 0) return NVQ_OK;
   if (!w || !codes_row || !scales_row || (dual && (!codes_col || !scales_col))) return NVQ_ERR_NULL;
-  if (!aligned(w, 16) || !aligned(codes_row, 16) || !aligned(scales_row, 16) ||
-      (dual && (!aligned(codes_col, 16) || !aligned(scales_col, 16))) ||
+  if (!aligned(w, 16) || !aligned(codes_row, 32) || !aligned(scales_row, 16) ||
+      (dual && (!aligned(codes_col, 32) || !aligned(scales_col, 16))) ||
       (status && !aligned(status, 4)))
     return NVQ_ERR_ALIGN;
   if ((rc = device_check())) return rc;
@@ -536,7 +536,7 @@ int mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16
   if (n < 0 || n % 32 || n >= (1ll << 46)) return NVQ_ERR_SHAPE;
   if (n == 0) return NVQ_OK;
   if (!codes || !scales || !dst) return NVQ_ERR_NULL;
-  if (!aligned(codes, 16) || !aligned(dst, 16)) return NVQ_ERR_ALIGN;
+  if (!aligned(codes, 16) || !aligned(dst, 32)) return NVQ_ERR_ALIGN;
   int rc = device_check();
   if (rc) return rc;
   return launch_result(nvq::launch_mx_dequant(codes, scales, n, dst, cs(stream)));

@@ -559,6 +559,20 @@ __device__ __forceinline__ void ldg32(const void* p, uint32_t v[8]) {
                : "l"(p));
 }
 
+// 32-byte store (one whole L2 sector per lane; 32-byte aligned address).
+__device__ __forceinline__ void stg256(void* p, const uint32_t v[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// The same with the streaming (evict-first) hint.
+__device__ __forceinline__ void stg256_stream(void* p, const uint32_t v[8]) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // Streaming 16-byte store (evict-first: the output is not read back soon).
 __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),

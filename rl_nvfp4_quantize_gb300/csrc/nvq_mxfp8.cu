@@ -36,17 +36,23 @@ __device__ __forceinline__ float mx_inv_scale(int s) {
 // (64 x 64 bf16, 128-byte swizzle) into one of two stages; the copy of the
 // next tile runs while the current one is quantised.
 //   rowwise pass   : warp w takes block column w (32 columns), lane l rows l
-//                    and l + 32: 32 codes (two 16-byte stores) and one scale
+//                    and l + 32: 32 codes (one 32-byte store) and one scale
 //                    byte per block;
 //   columnwise pass: thread t takes columns 2 (t & 127), +1 and rows
-//                    32 (t >> 7) .. +31: per column 32 codes (two 16-byte
-//                    stores into the transposed layout) and one scale byte.
+//                    32 (t >> 7) .. +31: per column 32 codes (one 32-byte
+//                    store into the transposed layout) and one scale byte.
+// Every code store fills one whole 32-byte L2 sector.  The scale bytes are
+// staged in shared memory and leave after the tile as one 8-byte store per
+// row (its 8 blocks) and one 2-byte store per column (its 2 blocks): written
+// one byte at a time, each would be a separate partial-sector write, and the
+// L2 write-operation rate, not DRAM bandwidth, bounded the kernel.
 // Inside a swizzled box, 16-byte chunk c of row r sits at chunk c ^ (r & 7).
 constexpr int kMxTR = 64, kMxTC = 256, kMxThreads = 256;
 constexpr int kMxBoxC = 64;
 constexpr int kMxBoxBytes = kMxTR * kMxBoxC * 2;  // 8 KiB
 constexpr int kMxStage = kMxTR * kMxTC * 2;       // 32 KiB
-constexpr int kMxSmem = 2 * kMxStage + 64;
+constexpr int kMxScaleStage = kMxTR * 8 + kMxTC * 2;  // row scales [64][8], column scales [256][2]
+constexpr int kMxSmem = 2 * kMxStage + kMxScaleStage + 64;
 constexpr int kMxMinBlocks = 3;
 constexpr uint32_t kMxWaitTries = 1u << 22;
 
@@ -74,7 +80,9 @@ __device__ __forceinline__ uint32_t e4m3x2_f32(float lo, float hi) {
 template <bool DUAL>
 __global__ void __launch_bounds__(kMxThreads, kMxMinBlocks) k_mx_tiles(const __grid_constant__ MxTileArgs A) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  uint64_t* const bar = reinterpret_cast<uint64_t*>(smem + 2 * kMxStage);
+  uint8_t* const srow = smem + 2 * kMxStage;    // [64 rows][8 blocks]
+  uint8_t* const scol = srow + kMxTR * 8;       // [256 columns][2 blocks]
+  uint64_t* const bar = reinterpret_cast<uint64_t*>(scol + kMxTC * 2);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {
     if (tid == 0 && A.status) atomicOr(A.status, kStatusTimeout);
@@ -158,14 +166,8 @@ __global__ void __launch_bounds__(kMxThreads, kMxMinBlocks) k_mx_tiles(const __g
             o[i] = e4m3x2_f32(a.x, a.y) | (e4m3x2_f32(c.x, c.y) << 16);
           }
           const int64_t grow = (int64_t)T.e * rows + T.r0 + r;
-          uint4* dst = reinterpret_cast<uint4*>(A.codes_row + grow * cols + T.c0 + 32 * b);
-          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          const int bc = (T.c0 >> 5) + b;
-          if (A.tiled)
-            A.scales_row[T.e * A.sl_row + scale_off_tiled(T.r0 + r, bc, A.ct_row)] = (uint8_t)(s + 127);
-          else
-            A.scales_row[grow * nb_row + bc] = (uint8_t)(s + 127);
+          stg256(A.codes_row + grow * cols + T.c0 + 32 * b, o);
+          srow[r * 8 + b] = (uint8_t)(s + 127);
         }
       }
     }
@@ -203,26 +205,62 @@ __global__ void __launch_bounds__(kMxThreads, kMxMinBlocks) k_mx_tiles(const __g
         }
         const int64_t gcol = (int64_t)T.e * cols + T.c0 + 2 * p;
         const int64_t r0 = T.r0 + 32 * rb;
-        uint4* dj = reinterpret_cast<uint4*>(A.codes_col + gcol * rows + r0);
-        uint4* dk = reinterpret_cast<uint4*>(A.codes_col + (gcol + 1) * rows + r0);
-        dj[0] = make_uint4(oj[0], oj[1], oj[2], oj[3]);
-        dj[1] = make_uint4(oj[4], oj[5], oj[6], oj[7]);
-        dk[0] = make_uint4(ok[0], ok[1], ok[2], ok[3]);
-        dk[1] = make_uint4(ok[4], ok[5], ok[6], ok[7]);
-        const int bc = (int)(r0 >> 5);
-        if (A.tiled) {
-          uint8_t* sc = A.scales_col + T.e * A.sl_col;
-          sc[scale_off_tiled(T.c0 + 2 * p, bc, A.ct_col)] = (uint8_t)(sj + 127);
-          sc[scale_off_tiled(T.c0 + 2 * p + 1, bc, A.ct_col)] = (uint8_t)(sk + 127);
-        } else {
-          A.scales_col[gcol * nb_col + bc] = (uint8_t)(sj + 127);
-          A.scales_col[(gcol + 1) * nb_col + bc] = (uint8_t)(sk + 127);
-        }
+        stg256(A.codes_col + gcol * rows + r0, oj);
+        stg256(A.codes_col + (gcol + 1) * rows + r0, ok);
+        scol[(2 * p) * 2 + rb] = (uint8_t)(sj + 127);
+        scol[(2 * p + 1) * 2 + rb] = (uint8_t)(sk + 127);
       }
     }
     if (inf && A.status) atomicOr(A.status, kStatusNonFinite);
     __syncthreads();
     issue(t + 2 * gridDim.x, st);
+
+    // scale write-out (the next iteration's barrier keeps the staging area
+    // until every thread has read it)
+    const int nbt = T.cv >> 5;        // blocks per row in this tile
+    const int bc0 = T.c0 >> 5;
+    if (tid < T.rv) {
+      const int r = tid;
+      const uint2 v = *reinterpret_cast<const uint2*>(srow + r * 8);
+      if (A.tiled) {
+        // block columns bc0 .. bc0 + 7: two runs of four bytes in two tiles
+        uint8_t* base = A.scales_row + T.e * A.sl_row;
+        if (nbt == 8) {
+          *reinterpret_cast<uint32_t*>(base + scale_off_tiled(T.r0 + r, bc0, A.ct_row)) = v.x;
+          *reinterpret_cast<uint32_t*>(base + scale_off_tiled(T.r0 + r, bc0 + 4, A.ct_row)) = v.y;
+        } else {
+          for (int b = 0; b < nbt; b++)
+            base[scale_off_tiled(T.r0 + r, bc0 + b, A.ct_row)] = srow[r * 8 + b];
+        }
+      } else {
+        uint8_t* d = A.scales_row + ((int64_t)T.e * rows + T.r0 + r) * nb_row + bc0;
+        if (nbt == 8 && (nb_row & 7) == 0) {
+          *reinterpret_cast<uint2*>(d) = v;
+        } else {
+          for (int b = 0; b < nbt; b++) d[b] = srow[r * 8 + b];
+        }
+      }
+    }
+    if (DUAL && tid < T.cv) {
+      const int c = tid, nrb = min(2, T.rv >> 5);
+      const int bc = T.r0 >> 5;     // even: tiles are 64 rows
+      const uint16_t v = *reinterpret_cast<const uint16_t*>(scol + c * 2);
+      if (A.tiled) {
+        uint8_t* base = A.scales_col + T.e * A.sl_col;
+        if (nrb == 2) {
+          *reinterpret_cast<uint16_t*>(base + scale_off_tiled(T.c0 + c, bc, A.ct_col)) = v;
+        } else {
+          base[scale_off_tiled(T.c0 + c, bc, A.ct_col)] = scol[c * 2];
+        }
+      } else {
+        uint8_t* d = A.scales_col + ((int64_t)T.e * cols + T.c0 + c) * nb_col + bc;
+        if (nrb == 2 && (nb_col & 1) == 0) {
+          *reinterpret_cast<uint16_t*>(d) = v;
+        } else {
+          for (int b = 0; b < nrb; b++) d[b] = scol[c * 2 + b];
+        }
+      }
+    }
   }
 }
 
@@ -305,9 +343,7 @@ __global__ void __launch_bounds__(kMxDqThreads)
         o[2 * k + h] = bf16x2_rn(y.x, y.y);
       }
     }
-    uint4* d = reinterpret_cast<uint4*>(dst + i * 16);
-    stg_stream(d, make_uint4(o[0], o[1], o[2], o[3]));
-    stg_stream(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+    stg256_stream(dst + i * 16, o);  // one whole sector
   }
 }
 
