@@ -132,7 +132,7 @@ constexpr int kColScales = 4 * kTC;             // [rb][col] 1 byte
 constexpr int kQuantSmem = 2 * kInStage + kColCodes + kColScales + kScaleTableBytes + 64;
 constexpr uint32_t kWaitTries = 1u << 22;
 
-struct __align__(64) QuantTileArgs {
+struct QuantTileArgs {  // aligned as CUtensorMap requires
   CUtensorMap tmap;       // w as [nexp * rows, cols] bf16, 64 x 64 boxes
   uint8_t* codes_row;
   uint8_t* scales_row;
@@ -559,13 +559,109 @@ __global__ void __launch_bounds__(kActThreads)
   }
 }
 
+// Short rows (H <= 2048: at most 4 blocks per lane) take one warp per
+// token: the row amax is a warp reduction with no CTA barrier, and each warp
+// keeps two rows in flight (one CTA per token kept too few loads in flight
+// per SM to cover the memory latency on such rows).
+constexpr int kActWarpThreads = 256;
+constexpr int kActWarpBlocks = 4;  // blocks per lane
+
+template <bool F46>
+__global__ void __launch_bounds__(kActWarpThreads)
+    k_act_warp(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
+               uint8_t* __restrict__ scales, float* __restrict__ token_scale,
+               int* __restrict__ status, int tiled) {
+  __shared__ ScaleEnt tbl[128];
+  build_scale_table(tbl);
+  __syncthreads();
+  const int nb = H / 16;
+  const int ct = (nb + 3) / 4;  // tiled layout: tiles per tile row
+  const int lane = threadIdx.x & 31;
+  const float six_m = F46 ? 1536.0f : 2688.0f;
+  const int64_t nwarps = (int64_t)gridDim.x * (kActWarpThreads / 32);
+  // the next row's blocks are loaded while this row is quantised, so each
+  // warp keeps two rows in flight
+  auto load = [&](int64_t row, uint32_t w[kActWarpBlocks][8]) {
+#pragma unroll
+    for (int k = 0; k < kActWarpBlocks; k++) {
+      const int b = lane + 32 * k;
+      if (row < T && b < nb) {
+        const uint4 lo = ldg_stream(x + row * H + b * 16);
+        const uint4 hi = ldg_stream(x + row * H + b * 16 + 8);
+        w[k][0] = lo.x; w[k][1] = lo.y; w[k][2] = lo.z; w[k][3] = lo.w;
+        w[k][4] = hi.x; w[k][5] = hi.y; w[k][6] = hi.z; w[k][7] = hi.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; i++) w[k][i] = 0;
+      }
+    }
+  };
+  int64_t row = blockIdx.x * (int64_t)(kActWarpThreads / 32) + (threadIdx.x >> 5);
+  uint32_t wr[kActWarpBlocks][8], wn[kActWarpBlocks][8];
+  load(row, wr);
+  for (; row < T; row += nwarps) {
+    load(row + nwarps, wn);
+    uint32_t bm[kActWarpBlocks];
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < kActWarpBlocks; k++) {
+      uint32_t mk = 0;
+#pragma unroll
+      for (int i = 0; i < 8; i++) mk = umaxmag2(mk, wr[k][i]);
+      bm[k] = mk;
+      m = umaxmag2(m, mk);
+    }
+    uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
+    mm = __reduce_max_sync(0xffffffffu, mm);
+    const float am = __uint_as_float(mm);
+    float G, E;
+    global_scales(am, six_m, G, E);
+    if (lane == 0) {
+      token_scale[row] = G;
+      if (status && !isfinite(am)) atomicOr(status, kStatusNonFinite);
+    }
+#pragma unroll
+    for (int k = 0; k < kActWarpBlocks; k++) {
+      const int b = lane + 32 * k;
+      if (b < nb) {
+        uint32_t c0w, c1w, sb;
+        quant_row_block_amax<F46>(wr[k], amax_of(bm[k]), E, tbl, c0w, c1w, sb);
+        *reinterpret_cast<uint2*>(codes + row * (H / 2) + b * 8) = make_uint2(c0w, c1w);
+        scales[tiled ? scale_off_tiled(row, b, ct) : row * nb + b] = (uint8_t)sb;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kActWarpBlocks; k++)
+#pragma unroll
+      for (int i = 0; i < 8; i++) wr[k][i] = wn[k][i];
+  }
+}
+
 cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* codes,
                        uint8_t* scales, float* token_scale, int* status, bool tiled,
                        cudaStream_t s) {
   if (T == 0 || H == 0) return cudaSuccess;
   const DevInfo* di = device_info();
-  const int grid = (int)std::min<int64_t>(T, (int64_t)di->sms * 16);
   const int t = tiled ? 1 : 0;
+  if (H / 16 <= 32 * kActWarpBlocks) {
+    static int per_sm[2] = {0, 0};
+    if (per_sm[f46] == 0) {
+      cudaError_t err = f46 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                  &per_sm[1], k_act_warp<true>, kActWarpThreads, 0)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                  &per_sm[0], k_act_warp<false>, kActWarpThreads, 0);
+      if (err != cudaSuccess) return err;
+      per_sm[f46] = std::max(per_sm[f46], 1);
+    }
+    const int64_t need = (T + kActWarpThreads / 32 - 1) / (kActWarpThreads / 32);
+    const int g = (int)std::min<int64_t>(need, (int64_t)di->sms * per_sm[f46]);
+    if (f46)
+      k_act_warp<true><<<g, kActWarpThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
+    else
+      k_act_warp<false><<<g, kActWarpThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
+    return cudaGetLastError();
+  }
+  const int grid = (int)std::min<int64_t>(T, (int64_t)di->sms * 16);
   if (f46)
     k_act<true><<<grid, kActThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
   else
@@ -688,7 +784,7 @@ __device__ __forceinline__ void dqt_column_pair(const uint2 cw[8], const uint32_
                  __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632));
 }
 
-struct __align__(64) DequantTArgs {
+struct DequantTArgs {  // aligned as CUtensorMap requires
   CUtensorMap tmap;  // dst as [nexp][in][out] bf16, boxes of 64 x 256 x 1
   const uint8_t* codes;
   const uint8_t* scales;
