@@ -435,13 +435,22 @@ def main():
 
     per_call = []
     for j, (name, _, b, k) in enumerate(calls):
-        ms = statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps))
-        per_call.append((name, ms, b))
+        times = [ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)]
+        per_call.append((name, statistics.mean(times), b, statistics.median(times)))
     peak, peak_src = load_peaks()
     dom = max(per_call, key=lambda x: x[1])
     dom_gbs = dom[2] / (dom[1] / 1e3) / 1e9
-    breakdown = {n: {"ms": round(ms, 4), "GB/s": round(b / (ms / 1e3) / 1e9, 1),
-                     "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)} for n, ms, b in per_call}
+    elems = call_elements(wl)
+    breakdown = {}
+    for n, ms, b, med in per_call:
+        e = {"ms": round(ms, 4), "ms_median": round(med, 4), "GB/s": round(b / (ms / 1e3) / 1e9, 1),
+             "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)}
+        if n in elems:
+            e["Gelem/s"] = round(elems[n] / (ms / 1e3) / 1e9, 2)
+        dram = load_traffic(n)
+        if dram:
+            e["dram_over_algorithmic"] = round(dram / b, 3)
+        breakdown[n] = e
     st = int(wl.status.item())
 
     # end to end through the public API with host buffers
@@ -491,6 +500,20 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def call_elements(wl):
+    """Elements each step call processes (input elements; for the routed
+    dequant the elements of the hit experts)."""
+    n_gu = GATE_UP[0] * GATE_UP[1] * GATE_UP[2]
+    n_dn = DOWN[0] * DOWN[1] * DOWN[2]
+    out = {"nvfp4_quantize_dual[gate_up]": n_gu, "nvfp4_quantize_dual[down]": n_dn,
+           "nvfp4_dequant_t[gate_up]": n_gu, "nvfp4_dequant_t[down]": n_dn,
+           "nf4_quantize[gate_up]": n_gu,
+           "nf4_dequant_routed[gate_up]": int(wl.nhit.item()) * GATE_UP[1] * GATE_UP[2]}
+    for T, H in ACTS:
+        out["act_quantize_per_token[%dx%d]" % (T, H)] = T * H
+    return out
 
 
 # Instruction issue peak of the GPU: 152 SMs x 4 schedulers x one warp
