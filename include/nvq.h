@@ -14,10 +14,11 @@
  * ---------------------------------------
  *  - Pointers.  Every tensor argument is a DEVICE pointer on the current
  *    CUDA device, except where a comment says "host".  The caller owns and
- *    allocates every buffer; the library allocates nothing, keeps no state
- *    between calls and never synchronises the host.  Bulk buffers (bf16
- *    inputs and outputs, codes, scales, absmax) must be 16-byte aligned;
- *    FP32 and int32 arrays 4-byte aligned.
+ *    allocates every buffer; the library allocates nothing, keeps no data
+ *    between calls (only per-device setup flags of its kernels, set once,
+ *    atomically) and never synchronises the host.  Bulk buffers (bf16
+ *    inputs and outputs, codes, scales, absmax) must be 16-byte aligned
+ *    (32-byte where a call says so); FP32 and int32 arrays 4-byte aligned.
  *  - bf16 tensors are passed as uint16_t bit patterns.  Shapes are int64.
  *    An expert stack is row-major [nexp, rows, cols] with cols contiguous;
  *    for an expert weight used as F.linear(x, W[e]) rows = out, cols = in
@@ -40,7 +41,9 @@
  *    NVQ_STATUS_TIMEOUT when a bounded internal wait gave up.  Kernels never
  *    trap and never spin without a bound.
  *  - Calls on different streams that write the same buffers race; the
- *    library is otherwise thread-safe (it has no global mutable state).
+ *    library is otherwise thread-safe (its only global state is the
+ *    per-device setup flags, updated atomically), and each call works on
+ *    whichever device is current.
  */
 #ifndef NVQ_H
 #define NVQ_H

@@ -314,13 +314,12 @@ cudaError_t launch_grouped_gemm(const uint16_t* x, const int64_t* counts, int64_
                                 cudaStream_t s) {
   using G = GroupedGemm<P, SA, SB, OUT_BF16>;
   static_assert(G::kSmem <= 232448, "shared memory per CTA");
-  static int attr_done = 0;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<P, SA, SB, OUT_BF16>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
-    if (err != cudaSuccess) return err;
-    attr_done = 1;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t err = attr.run([] {
+    return cudaFuncSetAttribute(k_grouped_gemm<P, SA, SB, OUT_BF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+  });
+  if (err != cudaSuccess) return err;
   GroupedGemmArgs<typename P::Params> A;
   int64_t tok = 0, tiles = 0;
   const int tiles_n = N / kGN;

@@ -1,11 +1,51 @@
 // nvq_internal.h -- host-side launchers behind the C ABI (not exported).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvq {
+
+// Host-side setup done once per kernel and device (the dynamic shared-memory
+// limit is a property of a function on each device).  Safe to call from
+// several host threads: a race at most repeats the setup, which is harmless.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};  // bit d: device d
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t err = setup();
+    if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return err;
+  }
+};
+
+// A positive per-device value (an occupancy figure) computed once per device.
+struct PerDeviceInt {
+  std::atomic<int> v[64];
+  PerDeviceInt() {
+    for (auto& x : v) x.store(0, std::memory_order_relaxed);
+  }
+  // compute() returns the value (> 0) or a CUDA error through *err.
+  template <class F>
+  int get(F&& compute, cudaError_t* err) {
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+      const int x = v[dev].load(std::memory_order_acquire);
+      if (x > 0) return x;
+    }
+    const int x = compute(err);
+    if (*err == cudaSuccess && x > 0 && dev >= 0 && dev < 64) v[dev].store(x, std::memory_order_release);
+    return x;
+  }
+};
 
 struct FastDiv;
 

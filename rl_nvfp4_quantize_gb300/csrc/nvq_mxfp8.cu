@@ -274,16 +274,15 @@ cudaError_t launch_mx_tiles(const uint16_t* w, int64_t nexp, int rows, int cols,
   if (ntiles == 0) return cudaSuccess;
   if (ntiles >= (1ll << 31) - (1ll << 24) || nexp * (int64_t)rows >= (1ll << 31))
     return cudaErrorInvalidValue;
-  static int attr_done[2] = {0, 0};
+  static PerDeviceOnce attr[2];
   const bool dual = codes_col != nullptr;
-  if (!attr_done[dual]) {
-    cudaError_t err = dual ? cudaFuncSetAttribute(k_mx_tiles<true>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem)
-                           : cudaFuncSetAttribute(k_mx_tiles<false>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
-    if (err != cudaSuccess) return err;
-    attr_done[dual] = 1;
-  }
+  cudaError_t err = attr[dual].run([&] {
+    return dual ? cudaFuncSetAttribute(k_mx_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMxSmem)
+                : cudaFuncSetAttribute(k_mx_tiles<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMxSmem);
+  });
+  if (err != cudaSuccess) return err;
   MxTileArgs A;
   if (!encode_tmap_2d(&A.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, (uint64_t)cols,
                       (uint64_t)(nexp * rows), (uint64_t)cols * 2, kMxBoxC, kMxTR,

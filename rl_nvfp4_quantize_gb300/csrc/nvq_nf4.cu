@@ -139,23 +139,21 @@ __global__ void __launch_bounds__(kNqThreads)
 
 cudaError_t launch_nf4_quant(const uint16_t* w, int64_t n, uint8_t* codes, float* absmax,
                              int* status, cudaStream_t s) {
-  static int attr_done = 0;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_nf4_quant, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kNqSmem);
-    if (err != cudaSuccess) return err;
-    attr_done = 1;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t err = attr.run([] {
+    return cudaFuncSetAttribute(k_nf4_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, kNqSmem);
+  });
+  if (err != cudaSuccess) return err;
   const int64_t nhalf = n / 32;
   if (nhalf == 0) return cudaSuccess;
   const DevInfo* di = device_info();
-  static int per_sm = 0;  // resident CTAs per SM (registers and shared memory permitting)
-  if (per_sm == 0) {
-    cudaError_t err =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_nf4_quant, kNqThreads, kNqSmem);
-    if (err != cudaSuccess) return err;
-    per_sm = std::max(per_sm, 1);
-  }
+  static PerDeviceInt occupancy;  // resident CTAs per SM (registers and shared memory permitting)
+  const int per_sm = std::max(1, occupancy.get([](cudaError_t* e) {
+    int b = 0;
+    *e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_nf4_quant, kNqThreads, kNqSmem);
+    return b;
+  }, &err));
+  if (err != cudaSuccess) return err;
   const int grid =
       (int)std::min<int64_t>((nhalf + kNqThreads - 1) / kNqThreads, (int64_t)di->sms * per_sm);
   k_nf4_quant<<<grid, kNqThreads, kNqSmem, s>>>(w, nhalf, codes, absmax, status);
@@ -236,14 +234,12 @@ cudaError_t launch_nf4_dequant(const uint8_t* codes, const float* absmax, int64_
   make_fastdiv(fd.d, &fd.m, &fd.s);
   const DevInfo* di = device_info();
   const int grid = (int)std::min<int64_t>(nexp * cps, (int64_t)di->sms * 6);
-  static int attr_done = 0;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_nf4_dequant,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kNdTableBytes);
-    if (err != cudaSuccess) return err;
-    attr_done = 1;
-  }
+  static PerDeviceOnce attr;
+  const cudaError_t err = attr.run([] {
+    return cudaFuncSetAttribute(k_nf4_dequant, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kNdTableBytes);
+  });
+  if (err != cudaSuccess) return err;
   k_nf4_dequant<<<grid, kNdThreads, kNdTableBytes, s>>>(codes, absmax, nexp, per_slice, fd,
                                                         hit_list, n_hit, dst);
   return cudaGetLastError();
@@ -309,14 +305,12 @@ __global__ void __launch_bounds__(kUnThreads)
 
 cudaError_t launch_routed_union(const int32_t* topk, int64_t n_idx, int nexp, int32_t* hit_list,
                                 int32_t* n_hit, int* status, cudaStream_t s) {
-  static int attr_done = 0;
+  static PerDeviceOnce attr;
   const int smem = ((nexp + 15) / 16) * 16;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_routed_union,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
-    if (err != cudaSuccess) return err;
-    attr_done = 1;
-  }
+  const cudaError_t err = attr.run([] {
+    return cudaFuncSetAttribute(k_routed_union, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
+  });
+  if (err != cudaSuccess) return err;
   k_routed_union<<<1, kUnThreads, smem, s>>>(topk, n_idx, nexp, hit_list, n_hit, status);
   return cudaGetLastError();
 }

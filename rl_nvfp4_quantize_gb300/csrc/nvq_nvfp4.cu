@@ -378,15 +378,11 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
 
 template <bool F46, bool DUAL>
 static cudaError_t set_quant_smem() {
-  static int attr_done = 0;  // per process; the attribute is per function
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_quant_tiles<F46, DUAL>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kQuantSmem);
-    if (err != cudaSuccess) return err;
-    attr_done = 1;
-  }
-  return cudaSuccess;
+  static PerDeviceOnce attr;
+  return attr.run([] {
+    return cudaFuncSetAttribute(k_quant_tiles<F46, DUAL>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
+  });
 }
 
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
@@ -644,17 +640,19 @@ cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* c
   const DevInfo* di = device_info();
   const int t = tiled ? 1 : 0;
   if (H / 16 <= 32 * kActWarpBlocks) {
-    static int per_sm[2] = {0, 0};
-    if (per_sm[f46] == 0) {
-      cudaError_t err = f46 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                  &per_sm[1], k_act_warp<true>, kActWarpThreads, 0)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                  &per_sm[0], k_act_warp<false>, kActWarpThreads, 0);
-      if (err != cudaSuccess) return err;
-      per_sm[f46] = std::max(per_sm[f46], 1);
-    }
+    static PerDeviceInt occupancy[2];
+    cudaError_t err = cudaSuccess;
+    const int per_sm = std::max(1, occupancy[f46].get([&](cudaError_t* e) {
+      int b = 0;
+      *e = f46 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_act_warp<true>,
+                                                               kActWarpThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_act_warp<false>,
+                                                               kActWarpThreads, 0);
+      return b;
+    }, &err));
+    if (err != cudaSuccess) return err;
     const int64_t need = (T + kActWarpThreads / 32 - 1) / (kActWarpThreads / 32);
-    const int g = (int)std::min<int64_t>(need, (int64_t)di->sms * per_sm[f46]);
+    const int g = (int)std::min<int64_t>(need, (int64_t)di->sms * per_sm);
     if (f46)
       k_act_warp<true><<<g, kActWarpThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
     else
@@ -870,13 +868,11 @@ __global__ void __launch_bounds__(kTqThreads, NVQ_TQ_MINB) k_dequant_t(const __g
 
 cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const float* G,
                              int64_t nexp, int out, int in, uint16_t* dst, cudaStream_t s) {
-  static int attr_done = 0;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(k_dequant_t, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kTqSmem);
-    if (err != cudaSuccess) return err;
-    attr_done = 1;
-  }
+  static PerDeviceOnce attr;
+  const cudaError_t err0 = attr.run([] {
+    return cudaFuncSetAttribute(k_dequant_t, cudaFuncAttributeMaxDynamicSharedMemorySize, kTqSmem);
+  });
+  if (err0 != cudaSuccess) return err0;
   const DevInfo* di = device_info();
   const int tiles_r = (out + kTqR - 1) / kTqR, tiles_c = (in + kTqC - 1) / kTqC;
   const int64_t ntiles = nexp * tiles_r * tiles_c;
