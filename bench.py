@@ -575,7 +575,9 @@ def measure_context(wl, dev, peak):
       * one bf16 weight [512, 256], no Four-Over-Six: quantise + dequantise,
         launch-bound, in microseconds per pair of calls;
       * dual-layout NVFP4 + Four-Over-Six of a 32-expert gate_up stack
-        [32, 4096, 6144] (the first 32 slices of the layer's stack);
+        [32, 4096, 6144] (the first 32 slices of the layer's stack), the
+        rowwise-only quantisation (with and without Four-Over-Six) and the
+        rowwise dequantisation of the same stack;
       * routed NF4 dequant for 8, 32 and 128 tokens of the same top-8 Zipf(1.1)
         router: how many of the 256 experts are hit and what that costs."""
     import torch
@@ -611,6 +613,21 @@ def measure_context(wl, dev, peak):
     gbs = (2 * n + 2 * nvfp4_bytes(n) + 8 * E) / (ms / 1e3) / 1e9
     out["dual_%dx%dx%d" % (E, R, K)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
                                         "frac": round(gbs / peak, 4)}
+    # rowwise-only quantisation (with and without Four-Over-Six) and the
+    # rowwise dequantisation of the same stack
+    qr = {"codes": q32["codes_row"], "scales": q32["scales_row"], "amax": q32["amax"],
+          "tensor_scale": q32["tensor_scale"]}
+    for f46 in (False, True):  # Four-Over-Six last: the buffers end as the dual call left them
+        ms = timed(lambda: nvq.nvfp4_quantize(wl.gu[:E], four_over_six=f46, out=qr), 5)
+        gbs = (2 * n + nvfp4_bytes(n) + 8 * E) / (ms / 1e3) / 1e9
+        out["rowwise%s_%dx%dx%d" % ("_4over6" if f46 else "", E, R, K)] = {
+            "ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    dq = torch.empty((E, R, K), dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: nvq.nvfp4_dequant(qr["codes"], qr["scales"], qr["tensor_scale"], out=dq), 5)
+    gbs = (nvfp4_bytes(n) + 2 * n + 4 * E) / (ms / 1e3) / 1e9
+    out["dequant_%dx%dx%d" % (E, R, K)] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                           "frac": round(gbs / peak, 4)}
+    del dq
     routed = {}
     per = R * K
     for T in (8, 32, 128):
