@@ -13,7 +13,9 @@ interpreter lock, so the tasks run on all host cores):
   * per-token NVFP4 + Four-Over-Six of activations [16384, 6144] and
     [32768, 2048];
   * NF4 of the 256-expert gate_up stack [256, 4096, 6144] and the routed
-    dequant of an 8192-token top-8 Zipf(1.1) router (all 256 experts hit).
+    dequant of an 8192-token top-8 Zipf(1.1) router (all 256 experts hit);
+  * MXFP8 rowwise + columnwise of the 32-expert stack [32, 4096, 6144] and
+    the dequant of its rowwise copy.
 
 Every code byte, scale byte, FP32 scale and absmax, every bf16 output and the
 hit list must be identical.
@@ -159,3 +161,28 @@ def test_nf4_256_experts_and_routed_dequant_every_element(nvq, oracle_mod):
         _run([lambda i=i: one(i) for i in range(min(chunk, E - e0))])
     del w, q, d
     torch.cuda.empty_cache()
+
+
+def test_mxfp8_32_experts_every_element(nvq, oracle_mod):
+    from rl_nvfp4_quantize_gb300 import synth
+    E, R, K = 32, 4096, 6144
+    w = synth.expert_weights(E, R, K, seed=23, device="cuda")
+    q = nvq.mxfp8_quantize(w, columnwise=True)
+    d = nvq.mxfp8_dequant(q["codes_row"], q["scales_row"])
+    torch.cuda.synchronize()
+    wh = u16(w)
+    h = {k: v.cpu().numpy() for k, v in q.items()}
+    dh = u16(d)
+    del w, q, d
+    torch.cuda.empty_cache()
+
+    def one(e):
+        x = wh[e:e + 1]
+        o = oracle_mod.mxfp8_quantize(x)
+        _same(h["codes_row"][e:e + 1], o["codes"], "mx codes_row[%d]" % e)
+        _same(h["scales_row"][e:e + 1], o["scales"], "mx scales_row[%d]" % e)
+        oc = oracle_mod.mxfp8_quantize_colwise(x)
+        _same(h["codes_col"][e:e + 1], oc["codes"], "mx codes_col[%d]" % e)
+        _same(h["scales_col"][e:e + 1], oc["scales"], "mx scales_col[%d]" % e)
+        _same(dh[e:e + 1], oracle_mod.mxfp8_dequant(o["codes"], o["scales"]), "mx dequant[%d]" % e)
+    _run([lambda e=e: one(e) for e in range(E)])
