@@ -154,6 +154,7 @@ struct QuantTileArgs {  // aligned as CUtensorMap requires
   int tiled;              // block scales in the tensor-core tiled layout
   int ct_row, ct_col;     // tiled layout: tiles per tile row (rowwise, columnwise)
   int64_t sl_row, sl_col; // tiled layout: bytes per slice (rowwise, columnwise)
+  int col32;              // codes_col is 32-byte aligned
 };
 
 template <bool F46, bool DUAL>
@@ -344,8 +345,15 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
           const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + c * 8);
           const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + c * 8);
           const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + c * 8);
-          reinterpret_cast<uint4*>(dstc)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
-          reinterpret_cast<uint4*>(dstc)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+          if (A.col32 && (rows & 63) == 0) {
+            // the run is 32-byte aligned: one full-sector store (half the
+            // write requests of two 16-byte stores)
+            const uint32_t v8[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+            stg256(dstc, v8);
+          } else {
+            reinterpret_cast<uint4*>(dstc)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+            reinterpret_cast<uint4*>(dstc)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+          }
         } else {
           for (int rb = 0; rb < nrb; rb++)
             *reinterpret_cast<uint2*>(dstc + rb * 8) =
@@ -423,6 +431,7 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
   A.ct_col = (rows / 16 + 3) / 4;
   A.sl_row = tiled_scale_bytes(rows, cols);
   A.sl_col = tiled_scale_bytes(cols, rows);
+  A.col32 = (reinterpret_cast<uintptr_t>(codes_col) & 31) == 0;
   const int full_grid = di->sms * NVQ_QT_MINB;
   // Slices per launch: with the look-ahead amax every launch quantises one
   // chunk while reducing the amax of the next, so each launch must see its

@@ -250,3 +250,17 @@ def test_misaligned_stack_falls_back(nvq, oracle_mod, monkeypatch):
     o = oracle_mod.nvfp4_quantize(u16(w), four_over_six=True)
     assert_same(u8(r["codes_row"]), o["codes"], "codes_row")
     assert_same(f32(r["amax"]).view(np.uint32), o["amax"].view(np.uint32), "amax")
+
+
+def test_codes_col_16_byte_aligned(nvq, oracle_mod):
+    """Columnwise codes into a buffer that is 16- but not 32-byte aligned take
+    the two 16-byte stores instead of one 32-byte store; both give the same
+    bytes."""
+    w = weights((2, 128, 512), seed=78)
+    buf = torch.empty(2 * 512 * 64 + 16, dtype=torch.uint8, device="cuda")
+    cc = buf[16:].view(2, 512, 64)
+    assert cc.data_ptr() % 32 == 16
+    r = nvq.nvfp4_quantize_dual(w.cuda(), four_over_six=True, out={"codes_col": cc})
+    ocol = oracle_mod.nvfp4_quantize_colwise(u16(w), four_over_six=True)
+    assert_same(u8(cc), ocol["codes"], "codes_col")
+    assert_same(u8(r["scales_col"]), ocol["scales"], "scales_col")
