@@ -10,7 +10,10 @@ arrays.  Every function cites the source passage it restates in the C file.
 
 Parity status: all functions are pinned by host tests; the NF4 level table is
 "parity unpinned" against third-party tables (it is derived here from the
-published normal-quantile construction).
+published normal-quantile construction).  The nested absmax follows the
+published double quantisation with the readings stated in the C file; its
+equality with any third-party nested code (whose 8-bit table differs) is not
+claimed.
 """
 from __future__ import annotations
 
@@ -101,6 +104,14 @@ def _load():
                 f.argtypes = [P, i64, i64, i64, P, P]
             lib.oracle_mxfp8_dequant.restype = None
             lib.oracle_mxfp8_dequant.argtypes = [P, P, i64, P]
+            lib.oracle_tree_sum.restype = C.c_float
+            lib.oracle_tree_sum.argtypes = [P, i64]
+            lib.oracle_absmax_mean.restype = C.c_float
+            lib.oracle_absmax_mean.argtypes = [P, i64]
+            lib.oracle_nf4_absmax_nest.restype = None
+            lib.oracle_nf4_absmax_nest.argtypes = [P, i64, i64, P, P, P]
+            lib.oracle_nf4_absmax_unnest.restype = None
+            lib.oracle_nf4_absmax_unnest.argtypes = [P, P, P, i64, i64, P]
             lib.oracle_nf4_dequant_routed.restype = None
             lib.oracle_nf4_dequant_routed.argtypes = [P, P, i64, i64, i64, P, i64, i64, P, P, P, P]
             _lib = lib
@@ -473,3 +484,40 @@ def mxfp8_values(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     e4 = np.array([e4m3_value(c) for c in range(256)], np.float64)
     sc = np.ldexp(1.0, np.asarray(scales, np.int64) - 127)
     return e4[np.asarray(codes, np.uint8)] * np.repeat(sc, 32, axis=-1)
+
+
+def tree_sum(a: np.ndarray) -> np.float32:
+    """Pairwise tree sum in binary32, zero padded to a power of two."""
+    a = np.ascontiguousarray(a, dtype=np.float32).ravel()
+    return np.float32(_load().oracle_tree_sum(_p(a), a.size))
+
+
+def absmax_mean(a: np.ndarray) -> np.float32:
+    a = np.ascontiguousarray(a, dtype=np.float32).ravel()
+    return np.float32(_load().oracle_absmax_mean(_p(a), a.size))
+
+
+def nf4_absmax_nest(absmax: np.ndarray):
+    """Nested (double-quantised) absmax of each expert slice: absmax [nexp, ...]
+    (FP32) -> codes [nexp, n] (E4M3 bytes), c1 [nexp, ceil(n/256)], mean [nexp]."""
+    a = np.ascontiguousarray(absmax, dtype=np.float32)
+    E = a.shape[0]
+    n = a.size // E if E else 0
+    nb = (n + 255) // 256
+    codes = np.zeros((E, n), np.uint8)
+    c1 = np.zeros((E, nb), np.float32)
+    mean = np.zeros(E, np.float32)
+    _load().oracle_nf4_absmax_nest(_p(a), E, n, _p(codes), _p(c1), _p(mean))
+    return dict(codes=codes, c1=c1, mean=mean)
+
+
+def nf4_absmax_unnest(codes: np.ndarray, c1: np.ndarray, mean: np.ndarray) -> np.ndarray:
+    """FP32 absmax [nexp, n] decoded from the nested form."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    c1 = np.ascontiguousarray(c1, dtype=np.float32)
+    mean = np.ascontiguousarray(mean, dtype=np.float32)
+    E = codes.shape[0]
+    n = codes.size // E if E else 0
+    out = np.zeros((E, n), np.float32)
+    _load().oracle_nf4_absmax_unnest(_p(codes), _p(c1), _p(mean), E, n, _p(out))
+    return out

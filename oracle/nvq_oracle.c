@@ -17,7 +17,8 @@
  *        (humans&), "Key claims" and "Method" (round-to-nearest, Four-Over-Six,
  *        per-token FP32 activation scales, FP32 error accumulation).
  *   [P5] "nf4moe -- QLoRA for a 743B Fused-MoE", "The fix: dequant-on-forward
- *        for routed experts" (NF4, blocksize 64, routed dequantisation).
+ *        for routed experts" (NF4, blocksize 64, routed dequantisation, the
+ *        "nested code" of the NF4 state).
  *
  * Where the sources leave a step open, the reading taken is stated at the
  * step.  Build: gcc -O2 -ffp-contract=off -fno-fast-math.  With contraction
@@ -659,4 +660,82 @@ ORACLE_API void oracle_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales
 {
     for (int64_t i = 0; i < n; i++)
         dst[i] = oracle_f32_to_bf16(ldexpf(oracle_e4m3_value(codes[i]), (int)scales[i / 32] - 127));
+}
+
+/* ------------------------------------------------------------------------ */
+/* NF4 double-quantised ("nested") absmax                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * [P5] "The fix" names the NF4 quantisation state as holding the absmax and
+ * a "nested code", and says no more.  The reading taken is the published
+ * double quantisation of QLoRA (Dettmers et al., 2023, "Double
+ * Quantization"): the first-level FP32 absmax values of one expert slice are
+ * centred on their mean and quantised again to 8-bit floats in blocks of
+ * 256.  Where that description is silent:
+ *   - the mean is the FP32 sum of the slice's n absmax values taken as a
+ *     pairwise tree (values padded with zeros to the next power of two,
+ *     adjacent pairs added level by level), divided by n in binary64 and
+ *     rounded to binary32;
+ *   - the 8-bit float is OCP E4M3, and each block's largest centred
+ *     magnitude c1 is mapped to 448 with the factor k = min(fl(448 / c1),
+ *     FLT_MAX) (the same encode-by-multiplication as the NVFP4 global scale);
+ *     codes are nearest-even, saturating, sign kept;
+ *   - decoding is one fused multiply-add: value(code) * fl(c1 / 448) + mean.
+ */
+
+/* Pairwise tree sum of a[0..n-1] in binary32, zero padded to a power of two. */
+ORACLE_API float oracle_tree_sum(const float* a, int64_t n)
+{
+    if (n <= 0) return 0.0f;
+    int64_t P = 1;
+    while (P < n) P *= 2;
+    float* s = (float*)calloc((size_t)P, sizeof(float));
+    if (!s) abort();
+    memcpy(s, a, (size_t)n * sizeof(float));
+    for (int64_t len = P; len > 1; len /= 2)
+        for (int64_t i = 0; i < len / 2; i++) s[i] = s[2 * i] + s[2 * i + 1];
+    float r = s[0];
+    free(s);
+    return r;
+}
+
+ORACLE_API float oracle_absmax_mean(const float* a, int64_t n)
+{
+    if (n <= 0) return 0.0f;
+    return (float)((double)oracle_tree_sum(a, n) / (double)n);
+}
+
+/* absmax [nexp, n] -> codes [nexp, n], c1 [nexp, ceil(n/256)], mean [nexp]. */
+ORACLE_API void oracle_nf4_absmax_nest(const float* absmax, int64_t nexp, int64_t n,
+                                       uint8_t* codes, float* c1, float* mean)
+{
+    const int64_t nb = (n + 255) / 256;
+    for (int64_t e = 0; e < nexp; e++) {
+        const float* a = absmax + e * n;
+        const float mu = oracle_absmax_mean(a, n);
+        mean[e] = mu;
+        for (int64_t b = 0; b < nb; b++) {
+            const int64_t i0 = 256 * b, i1 = (i0 + 256 < n) ? i0 + 256 : n;
+            float m = 0.0f;
+            for (int64_t i = i0; i < i1; i++) {
+                float v = fabsf(a[i] - mu);
+                if (v > m) m = v;
+            }
+            c1[e * nb + b] = m;
+            float k = 448.0f / m;
+            if (k > FLT_MAX) k = FLT_MAX;
+            for (int64_t i = i0; i < i1; i++) codes[e * n + i] = e4m3_signed((a[i] - mu) * k);
+        }
+    }
+}
+
+ORACLE_API void oracle_nf4_absmax_unnest(const uint8_t* codes, const float* c1, const float* mean,
+                                         int64_t nexp, int64_t n, float* absmax)
+{
+    const int64_t nb = (n + 255) / 256;
+    for (int64_t e = 0; e < nexp; e++)
+        for (int64_t i = 0; i < n; i++) {
+            const float r = c1[e * nb + i / 256] / 448.0f;
+            absmax[e * n + i] = fmaf(oracle_e4m3_value(codes[e * n + i]), r, mean[e]);
+        }
 }
