@@ -239,6 +239,45 @@ NVQ_API int nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp,
                 int64_t cols, uint16_t* dst, nvq_stream_t stream);
 
 /*
+ * nf4_absmax_nest -- the nested ("double-quantised") form of NF4 absmax
+ * values ([P5] "The fix": the NF4 state holds the absmax and a "nested
+ * code"), read as QLoRA's double quantisation (Dettmers et al., 2023,
+ * "Double Quantization"), per expert slice of n = nblocks absmax values:
+ *   mean    = RN32(RN64(S / n)), S = the FP32 pairwise-tree sum of the n
+ *             values (zero padded to a power of two, adjacent pairs added
+ *             level by level; the result does not depend on the launch);
+ *   v_i     = fl(absmax_i - mean);
+ *   c1_b    = max |v_i| over block b of 256 consecutive values (the last
+ *             block of a slice may be shorter);
+ *   code_i  = E4M3(fl(v_i * k_b)), k_b = min(fl(448 / c1_b), FLT_MAX),
+ *             nearest-even, saturating at 448, sign kept.
+ * Decoding (nf4_absmax_unnest): absmax'_i = fma(value(code_i), fl(c1_b/448),
+ * mean).  1 byte + 4/256 bytes per NF4 block instead of 4.
+ *
+ *   absmax  in   f32 [nexp, nblocks] (4-byte aligned; e.g. nf4_quantize's
+ *                absmax with nblocks = rows * cols / 64)
+ *   codes   out  u8 [nexp, nblocks] (E4M3 bytes)
+ *   c1      out  f32 [nexp, ceil(nblocks / 256)]
+ *   mean    out  f32 [nexp]
+ *   status  out  nullable; NVQ_STATUS_NONFINITE for a non-finite mean or c1
+ * nblocks <= 2^25 (NVQ_ERR_SHAPE otherwise).  nblocks == 0 writes mean = 0.
+ */
+NVQ_API int nf4_absmax_nest(const float* absmax, int64_t nexp, int64_t nblocks, uint8_t* codes,
+                            float* c1, float* mean, int* status, nvq_stream_t stream);
+
+/*
+ * nf4_absmax_unnest -- FP32 absmax decoded from the nested form (above):
+ * absmax[e, i] = fma(E4M3 value of codes[e, i], fl(c1[e, i / 256] / 448),
+ * mean[e]).  The result feeds nf4_dequant, nf4_dequant_routed and
+ * nf4_routed_linear as their absmax.
+ *
+ *   codes, c1, mean  in   as written by nf4_absmax_nest
+ *   absmax           out  f32 [nexp, nblocks] (4-byte aligned)
+ */
+NVQ_API int nf4_absmax_unnest(const uint8_t* codes, const float* c1, const float* mean,
+                              int64_t nexp, int64_t nblocks, float* absmax, nvq_stream_t stream);
+
+/*
  * nf4_dequant_routed -- dequant-on-forward of only the experts the router hit
  * ([P5] "The fix": the union of top_k_index is formed once, and only those
  * experts are dequantised).  The union is computed on the device and consumed

@@ -25,6 +25,7 @@ __all__ = [
     "NvqError", "FLAG_4OVER6", "FLAG_AMAX_GIVEN", "FLAG_SCALES_SWIZZLED", "STATUS_NONFINITE", "STATUS_BAD_INDEX", "STATUS_TIMEOUT",
     "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_dequant", "nvfp4_dequant_t", "nvfp4_dgrad",
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed", "nf4_routed_linear",
+    "nf4_absmax_nest", "nf4_absmax_unnest",
     "mxfp8_quantize", "mxfp8_dequant", "mx_scale_bytes",
     "nf4_codebook", "scale_bytes", "debug_convert", "debug_wait_timeout", "lib", "library_path",
 ]
@@ -73,6 +74,8 @@ def _load():
         "mxfp8_quantize": ([P, i64, i64, i64, u32, P, P, P, P, P, P], i32),
         "mxfp8_dequant": ([P, P, i64, P, P], i32),
         "nvq_mx_scale_bytes": ([i64, i64, u32], i64),
+        "nf4_absmax_nest": ([P, i64, i64, P, P, P, P, P], i32),
+        "nf4_absmax_unnest": ([P, P, P, i64, i64, P, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -245,6 +248,33 @@ def nf4_dequant(codes, absmax, stream=None, out=None):
     _check("nf4_dequant", lib.nf4_dequant(_ptr(codes), _ptr(absmax), E, R, K, _ptr(dst),
                                           _stream(stream)))
     return dst
+
+
+def nf4_absmax_nest(absmax, status=None, stream=None, out=None):
+    """Nested (double-quantised) form of NF4 absmax [nexp, ...] (FP32):
+    codes u8 [nexp, n], c1 f32 [nexp, ceil(n/256)], mean f32 [nexp]."""
+    if absmax.dtype != torch.float32:
+        raise TypeError("absmax must be float32")
+    a = absmax.contiguous()
+    E = a.shape[0]
+    n = a.numel() // E if E else 0
+    o = out or {}
+    codes = o.get("codes", _empty((E, n), torch.uint8, a))
+    c1 = o.get("c1", _empty((E, (n + 255) // 256), torch.float32, a))
+    mean = o.get("mean", _empty((E,), torch.float32, a))
+    _check("nf4_absmax_nest", lib.nf4_absmax_nest(_ptr(a), E, n, _ptr(codes), _ptr(c1), _ptr(mean),
+                                                  _ptr(status), _stream(stream)))
+    return dict(codes=codes, c1=c1, mean=mean)
+
+
+def nf4_absmax_unnest(codes, c1, mean, shape=None, stream=None, out=None):
+    """FP32 absmax decoded from the nested form, [nexp, n] (or `shape`)."""
+    E = codes.shape[0]
+    n = codes.numel() // E if E else 0
+    dst = out if out is not None else _empty((E, n), torch.float32, codes)
+    _check("nf4_absmax_unnest", lib.nf4_absmax_unnest(_ptr(codes), _ptr(c1), _ptr(mean), E, n,
+                                                      _ptr(dst), _stream(stream)))
+    return dst.view(shape) if shape is not None else dst
 
 
 def nf4_dequant_routed(codes, absmax, topk_idx, dst=None, status=None, stream=None,

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libnvq.so")
 SOURCES = ["nvq_api.cu", "nvq_nvfp4.cu", "nvq_nf4.cu", "nvq_dgrad.cu", "nvq_nf4_linear.cu",
-           "nvq_mxfp8.cu"]
+           "nvq_mxfp8.cu", "nvq_nf4_nest.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",

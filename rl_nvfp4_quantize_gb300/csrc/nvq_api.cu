@@ -372,6 +372,37 @@ int nf4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, ui
   return launch_result(nvq::launch_nf4_quant(w, total, codes, absmax, status, cs(stream)));
 }
 
+int nf4_absmax_nest(const float* absmax, int64_t nexp, int64_t nblocks, uint8_t* codes, float* c1,
+                    float* mean, int* status, nvq_stream_t stream) {
+  int64_t total;
+  if (nexp < 0 || nblocks < 0 || !mul_ok(nexp, nblocks, 1, &total)) return NVQ_ERR_SHAPE;
+  if (nblocks > ((int64_t)1 << 25)) return NVQ_ERR_SHAPE;
+  if (nexp == 0) return NVQ_OK;
+  if (!mean) return NVQ_ERR_NULL;
+  if (total > 0 && (!absmax || !codes || !c1)) return NVQ_ERR_NULL;
+  if (!aligned(mean, 4) || (absmax && !aligned(absmax, 4)) || (c1 && !aligned(c1, 4)) ||
+      (status && !aligned(status, 4)))
+    return NVQ_ERR_ALIGN;
+  int rc;
+  if ((rc = device_check())) return rc;
+  if (nblocks == 0) return launch_result(cudaMemsetAsync(mean, 0, (size_t)nexp * 4, cs(stream)));
+  return launch_result(
+      nvq::launch_nf4_nest(absmax, nexp, nblocks, codes, c1, mean, status, cs(stream)));
+}
+
+int nf4_absmax_unnest(const uint8_t* codes, const float* c1, const float* mean, int64_t nexp,
+                      int64_t nblocks, float* absmax, nvq_stream_t stream) {
+  int64_t total;
+  if (nexp < 0 || nblocks < 0 || !mul_ok(nexp, nblocks, 4, &total)) return NVQ_ERR_SHAPE;
+  if (total == 0) return NVQ_OK;
+  if (!codes || !c1 || !mean || !absmax) return NVQ_ERR_NULL;
+  if (!aligned(c1, 4) || !aligned(mean, 4) || !aligned(absmax, 4)) return NVQ_ERR_ALIGN;
+  int rc;
+  if ((rc = device_check())) return rc;
+  return launch_result(
+      nvq::launch_nf4_unnest(codes, c1, mean, nexp, nblocks, absmax, cs(stream)));
+}
+
 int nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp, int64_t rows,
                 int64_t cols, uint16_t* dst, nvq_stream_t stream) {
   int64_t total;

@@ -155,5 +155,9 @@ cudaError_t launch_nf4_linear(const uint16_t* x, const int64_t* counts, int64_t 
 
 // The 16 NF4 levels used by the kernels (host copy).
 void nf4_levels_host(float out[16]);
+cudaError_t launch_nf4_nest(const float* absmax, int64_t nexp, int64_t n, uint8_t* codes,
+                            float* c1, float* mean, int* status, cudaStream_t s);
+cudaError_t launch_nf4_unnest(const uint8_t* codes, const float* c1, const float* mean,
+                              int64_t nexp, int64_t n, float* out, cudaStream_t s);
 
 }  // namespace nvq

@@ -11,6 +11,11 @@ describe; no dataset or checkpoint is used:
 * the 512 x 256 single weight, N(0, 0.02) with 0.1 % outliers x 20;
 * activations: Student-t (nu = 3) values times 0.5 with 8 outlier channels
   x 50 ("The 4-bitter Lesson" quantises activations per token);
+* NF4 block absmax values (the input of the nested absmax): for N(0, sigma)
+  weights the largest magnitude of 64 values sits near 2.4 sigma with a
+  spread of about 0.4 sigma, so sigma_e * max(0.5, 2.4 + 0.4 z), z ~ N(0, 1),
+  with sigma_e = 0.02 * u_e as for the weights, rounded to bf16 (the absmax
+  of bf16 weights is a bf16 value) and a small fraction of zero blocks;
 * router choices: top-8 of 256 experts per token with Zipf(1.1) popularity
   over a seeded permutation of the experts; each token draws 8 distinct
   experts by the Gumbel-top-k trick.
@@ -51,6 +56,17 @@ def expert_weights(nexp, rows, cols, seed, device="cpu", std=0.02, jitter=(0.5, 
             x[m] *= outlier_mult
         flat[e0:e1].copy_(x)
     return w
+
+
+def nf4_absmax_values(nexp, n, seed, device="cpu", zero_frac=0.0002):
+    """f32 [nexp, n]: bf16-representable block maxima, sigma_e * max(0.5, 2.4 + 0.4 z)."""
+    g = _gen(device, seed)
+    u = torch.empty(nexp, device=device).uniform_(0.5, 2.0, generator=g)
+    z = torch.randn((nexp, n), device=device, generator=g)
+    a = (0.02 * u.unsqueeze(1)) * torch.clamp(2.4 + 0.4 * z, min=0.5)
+    if zero_frac > 0:
+        a[torch.rand((nexp, n), device=device, generator=g) < zero_frac] = 0.0
+    return a.to(torch.bfloat16).to(torch.float32)
 
 
 def single_weight(rows=512, cols=256, seed=0, device="cpu"):

@@ -162,6 +162,17 @@ def test_validation_before_any_device_work(nvq):
     assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(16, P, P) == 1
     assert L.nvq_debug_wait_timeout(16, _vp(FAKE + 2), P) == 2
+    # nested NF4 absmax
+    assert L.nf4_absmax_nest(ok16, 1, (1 << 25) + 1, ok16, ok16, ok16, P, P) == 3
+    assert L.nf4_absmax_nest(ok16, -1, 8, ok16, ok16, ok16, P, P) == 3
+    assert L.nf4_absmax_nest(ok16, 2, 8, ok16, ok16, P, P, P) == 1
+    assert L.nf4_absmax_nest(P, 2, 8, ok16, ok16, ok16, P, P) == 1
+    assert L.nf4_absmax_nest(ok16, 2, 8, ok16, _vp(FAKE + 2), ok16, P, P) == 2
+    assert L.nf4_absmax_nest(P, 0, 8, P, P, P, P, P) == 0
+    assert L.nf4_absmax_unnest(ok16, ok16, ok16, 2, 8, P, P) == 1
+    assert L.nf4_absmax_unnest(ok16, ok16, _vp(FAKE + 1), 2, 8, ok16, P) == 2
+    assert L.nf4_absmax_unnest(ok16, ok16, ok16, 2, -8, ok16, P) == 3
+    assert L.nf4_absmax_unnest(P, P, P, 2, 0, P, P) == 0
 
 
 def test_valid_call_without_gpu_reports_device(nvq):
@@ -171,3 +182,5 @@ def test_valid_call_without_gpu_reports_device(nvq):
     ok16 = _vp(FAKE)
     assert nvq.lib.nvfp4_quantize(ok16, 1, 16, 16, 0, ok16, ok16, ok16, ok16, P, P) == 5
     assert nvq.lib.nf4_dequant_routed(ok16, ok16, 4, 4, 64, ok16, 2, 2, ok16, ok16, ok16, P, P) == 5
+    assert nvq.lib.nf4_absmax_nest(ok16, 2, 8, ok16, ok16, ok16, P, P) == 5
+    assert nvq.lib.nf4_absmax_unnest(ok16, ok16, ok16, 2, 8, ok16, P) == 5
