@@ -368,7 +368,7 @@ def main():
                     help="skip the context measurements outside the step")
     ap.add_argument("--unfused", action="store_true",
                     help="with --case: also time the dequant + per-expert cuBLAS comparison")
-    ap.add_argument("--case", default=None, choices=["dgrad", "nf4_linear", "mxfp8"],
+    ap.add_argument("--case", default=None, choices=["dgrad", "nf4_linear", "mxfp8", "nest"],
                     help="run one context measurement alone on a reduced case (profiling)")
     ap.add_argument("--tokens", type=int, default=2048,
                     help="router tokens of --case")
@@ -646,7 +646,33 @@ def measure_context(wl, dev, peak):
         {"gate_up": (wl.nf4["codes"], wl.nf4["absmax"], GATE_UP)}, wl.topk, dev)
     out["swizzled_scales"] = measure_swizzled(wl, dev, peak)
     out["mxfp8"] = measure_mxfp8(wl, peak)
+    out["nf4_absmax_nested"] = measure_nest(wl, peak)
     return out
+
+
+def measure_nest(wl, peak):
+    """The nested (double-quantised) NF4 absmax (row F4) of the whole gate_up
+    stack's absmax, [256, 4096 x 6144 / 64] FP32: nf4_absmax_nest (4 B in;
+    1 B code + 4/256 B block maximum out per value) and nf4_absmax_unnest
+    (the reverse)."""
+    import torch
+    import rl_nvfp4_quantize_gb300 as nvq
+    a = wl.nf4["absmax"]
+    E = a.shape[0]
+    n = a.numel() // E
+    nb = (n + 255) // 256
+    nest = nvq.nf4_absmax_nest(a)
+    ms = cuda_timed(lambda: nvq.nf4_absmax_nest(a, out=nest), 5)
+    b = 4 * E * n + E * n + 4 * E * nb + 4 * E
+    res = {"nest_%dx%d" % (E, n): {"ms": round(ms, 4), "GB/s": round(b / (ms / 1e3) / 1e9, 1),
+                                   "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)}}
+    dst = torch.empty((E, n), dtype=torch.float32, device=a.device)
+    ms = cuda_timed(lambda: nvq.nf4_absmax_unnest(nest["codes"], nest["c1"], nest["mean"], out=dst), 5)
+    res["unnest_%dx%d" % (E, n)] = {"ms": round(ms, 4), "GB/s": round(b / (ms / 1e3) / 1e9, 1),
+                                    "frac": round(b / (ms / 1e3) / 1e9 / peak, 4)}
+    del nest, dst
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_mxfp8(wl, peak):
@@ -825,8 +851,9 @@ def run_case(args):
     --case nf4_linear quantises them to NF4; both route --tokens tokens top-8
     with the Zipf(1.1) router and time nvfp4_dgrad / nf4_routed_linear on
     both stacks (the cuBLAS comparison only with --unfused).  --case mxfp8
-    times the MXFP8 calls on a gate_up stack of --experts slices.  Prints one
-    JSON object."""
+    times the MXFP8 calls on a gate_up stack of --experts slices; --case nest
+    times the nested NF4 absmax of a gate_up stack of --experts slices.
+    Prints one JSON object."""
     import torch
     import rl_nvfp4_quantize_gb300 as nvq
     from rl_nvfp4_quantize_gb300 import synth
@@ -840,6 +867,14 @@ def run_case(args):
         wl.gu = synth.expert_weights(*GATE_UP, seed=2, device=dev)
         peak, _ = load_peaks()
         print(json.dumps({"case": args.case, "experts": E, "result": measure_mxfp8(wl, peak)}))
+        return
+    if args.case == "nest":
+        class _N:  # the NF4 state measure_nest reads
+            pass
+        wl = _N()
+        wl.nf4 = nvq.nf4_quantize(synth.expert_weights(*GATE_UP, seed=2, device=dev))
+        peak, _ = load_peaks()
+        print(json.dumps({"case": args.case, "experts": E, "result": measure_nest(wl, peak)}))
         return
     stacks = {}
     for name, shape, seed in (("gate_up", GATE_UP, 2), ("down", DOWN, 3)):
