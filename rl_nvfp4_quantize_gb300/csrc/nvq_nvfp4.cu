@@ -129,7 +129,10 @@ constexpr int kBoxBytes = kTR * kBoxC * 2;      // 8 KiB
 constexpr int kInStage = kTR * kTC * 2;         // 32 KiB (four boxes)
 constexpr int kColCodes = 4 * kTC * 8;          // [rb][col] 8 bytes
 constexpr int kColScales = 4 * kTC;             // [rb][col] 1 byte
-constexpr int kQuantSmem = 2 * kInStage + kColCodes + kColScales + kScaleTableBytes + 64;
+constexpr int kColBuf = kColCodes + kColScales; // one tile's staged columnwise results
+// Shared memory of the rowwise-only (DUAL false) and dual-layout kernels.
+template <bool DUAL>
+constexpr int quant_smem() { return 2 * kInStage + (DUAL ? kColBuf : 0) + kScaleTableBytes + 64; }
 constexpr uint32_t kWaitTries = 1u << 22;
 
 struct QuantTileArgs {  // aligned as CUtensorMap requires
@@ -164,10 +167,10 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
   // require; a misaligned base is reported instead of used.
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* const in0 = smem;
-  unsigned char* const colc = smem + 2 * kInStage;
+  unsigned char* const colc = smem + 2 * kInStage;  // DUAL: kColBuf bytes
   unsigned char* const cols_s = colc + kColCodes;
-  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(cols_s + kColScales);
-  uint64_t* const bar = reinterpret_cast<uint64_t*>(cols_s + kColScales + kScaleTableBytes);
+  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(colc + (DUAL ? kColBuf : 0));
+  uint64_t* const bar = reinterpret_cast<uint64_t*>(colc + (DUAL ? kColBuf : 0) + kScaleTableBytes);
   float* const s_E = reinterpret_cast<float*>(bar + 2);
   const int tid = threadIdx.x;
   if (smem_u32(smem) & 1023u) {
@@ -236,15 +239,74 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
   const int cr = warp >> 1, q = ((warp & 1) << 5) + lane;
   const int cbox = (q >> 4) * kBoxBytes, cchunk = (q & 15) >> 1, chalf = (q & 1) * 8;
 
+  // The columnwise results of a tile, staged in shared memory (codes
+  // [rb][col] 8 bytes, then scales [rb][col] 1 byte), leave as contiguous
+  // runs of the transposed layout: thread c writes column c.
+  auto write_col = [&](const Tile& T) {
+    const int c = tid;
+    if (c < T.cv) {
+      const int nrb = T.rv >> 4;
+      const int64_t grow = (int64_t)T.e * cols + T.c0 + c;
+      uint8_t* dstc = A.codes_col + grow * rows_h + (T.r0 >> 1);
+      uint8_t* dsts = A.scales_col + grow * rows_16 + (T.r0 >> 4);
+      if (nrb == 4 && (rows & 31) == 0) {
+        const uint2 v0 = *reinterpret_cast<const uint2*>(colc + c * 8);
+        const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + c * 8);
+        const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + c * 8);
+        const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + c * 8);
+        if (A.col32 && (rows & 63) == 0) {
+          // the run is 32-byte aligned: one full-sector store (half the
+          // write requests of two 16-byte stores)
+          const uint32_t v8[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+          stg256(dstc, v8);
+        } else {
+          reinterpret_cast<uint4*>(dstc)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+          reinterpret_cast<uint4*>(dstc)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+        }
+      } else {
+        for (int rb = 0; rb < nrb; rb++)
+          *reinterpret_cast<uint2*>(dstc + rb * 8) =
+              *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + c * 8);
+      }
+      if (A.tiled) {
+        // the tile's four row blocks are block columns r0/16 .. +3, a
+        // multiple of 4: four consecutive bytes of one tiled row
+        uint8_t* dt = A.scales_col + T.e * A.sl_col +
+                      scale_off_tiled(T.c0 + c, T.r0 >> 4, A.ct_col);
+        if (nrb == 4) {
+          *reinterpret_cast<uint32_t*>(dt) =
+              (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
+              ((uint32_t)cols_s[2 * kTC + c] << 16) | ((uint32_t)cols_s[3 * kTC + c] << 24);
+        } else {
+          for (int rb = 0; rb < nrb; rb++) dt[rb] = cols_s[rb * kTC + c];
+        }
+      } else if (nrb == 4 && (rows & 63) == 0) {
+        const uint32_t sc = (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
+                            ((uint32_t)cols_s[2 * kTC + c] << 16) |
+                            ((uint32_t)cols_s[3 * kTC + c] << 24);
+        *reinterpret_cast<uint32_t*>(dsts) = sc;
+      } else {
+        for (int rb = 0; rb < nrb; rb++) dsts[rb] = cols_s[rb * kTC + c];
+      }
+    }
+  };
+
+  // The rowwise-only kernel has one barrier per tile: the barrier that
+  // opens tile t + 1 also frees tile t's input stage, which then takes the
+  // copy two tiles ahead.  The dual kernel needs a second barrier between
+  // the columnwise pass and the write-out of its staged results, and frees
+  // the stage there.
   int st = 0;
   uint32_t it = 0;
   for (uint32_t t = t0; t < A.ntiles; t += gridDim.x, st ^= 1, it++) {
     const bool ok = mbar_wait(&bar[st], (it >> 1) & 1, kWaitTries);
     if (__syncthreads_or(!ok)) {  // a copy never landed: report and stop
       if (tid == 0 && A.status) atomicOr(A.status, kStatusTimeout);
-      mbar_wait(&bar[st ^ 1], ((it + 1) >> 1) & 1, kWaitTries);
+      // the other stage's copy, if one is in flight
+      if (DUAL || it == 0) mbar_wait(&bar[st ^ 1], ((it + 1) >> 1) & 1, kWaitTries);
       return;
     }
+    if (!DUAL && it > 0) issue(t + gridDim.x, st ^ 1);
     const Tile T = tile_of(t);
     const float E = s_E[st];
     const unsigned char* tile = in0 + st * kInStage;
@@ -329,57 +391,9 @@ __global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_c
         sw |= (sbj << 16) | (sbk << 24);
         *reinterpret_cast<uint32_t*>(cols_s + cr * kTC + q * 4) = sw;
       }
-    }
-    __syncthreads();
-    issue(t + 2 * gridDim.x, st);
-
-    if (DUAL) {
-      const int c = tid;
-      if (c < T.cv) {
-        const int nrb = T.rv >> 4;
-        const int64_t grow = (int64_t)T.e * cols + T.c0 + c;
-        uint8_t* dstc = A.codes_col + grow * rows_h + (T.r0 >> 1);
-        uint8_t* dsts = A.scales_col + grow * rows_16 + (T.r0 >> 4);
-        if (nrb == 4 && (rows & 31) == 0) {
-          const uint2 v0 = *reinterpret_cast<const uint2*>(colc + c * 8);
-          const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + c * 8);
-          const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + c * 8);
-          const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + c * 8);
-          if (A.col32 && (rows & 63) == 0) {
-            // the run is 32-byte aligned: one full-sector store (half the
-            // write requests of two 16-byte stores)
-            const uint32_t v8[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
-            stg256(dstc, v8);
-          } else {
-            reinterpret_cast<uint4*>(dstc)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
-            reinterpret_cast<uint4*>(dstc)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
-          }
-        } else {
-          for (int rb = 0; rb < nrb; rb++)
-            *reinterpret_cast<uint2*>(dstc + rb * 8) =
-                *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + c * 8);
-        }
-        if (A.tiled) {
-          // the tile's four row blocks are block columns r0/16 .. +3, a
-          // multiple of 4: four consecutive bytes of one tiled row
-          uint8_t* dt = A.scales_col + T.e * A.sl_col +
-                        scale_off_tiled(T.c0 + c, T.r0 >> 4, A.ct_col);
-          if (nrb == 4) {
-            *reinterpret_cast<uint32_t*>(dt) =
-                (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
-                ((uint32_t)cols_s[2 * kTC + c] << 16) | ((uint32_t)cols_s[3 * kTC + c] << 24);
-          } else {
-            for (int rb = 0; rb < nrb; rb++) dt[rb] = cols_s[rb * kTC + c];
-          }
-        } else if (nrb == 4 && (rows & 63) == 0) {
-          const uint32_t sc = (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
-                              ((uint32_t)cols_s[2 * kTC + c] << 16) |
-                              ((uint32_t)cols_s[3 * kTC + c] << 24);
-          *reinterpret_cast<uint32_t*>(dsts) = sc;
-        } else {
-          for (int rb = 0; rb < nrb; rb++) dsts[rb] = cols_s[rb * kTC + c];
-        }
-      }
+      __syncthreads();
+      issue(t + 2 * gridDim.x, st);
+      write_col(T);
     }
   }
 }
@@ -389,7 +403,7 @@ static cudaError_t set_quant_smem() {
   static PerDeviceOnce attr;
   return attr.run([] {
     return cudaFuncSetAttribute(k_quant_tiles<F46, DUAL>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, quant_smem<DUAL>());
   });
 }
 
@@ -471,10 +485,10 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
     A.ntiles = (uint32_t)(n * per);
     A.ahead = (lookahead && e0 + chunk < nexp) ? (uint32_t)chunk : 0u;
     const int grid = (int)std::min<int64_t>(n * per, full_grid);
-    if (f46 && dual) k_quant_tiles<true, true><<<grid, kQT, kQuantSmem, s>>>(A);
-    else if (f46) k_quant_tiles<true, false><<<grid, kQT, kQuantSmem, s>>>(A);
-    else if (dual) k_quant_tiles<false, true><<<grid, kQT, kQuantSmem, s>>>(A);
-    else k_quant_tiles<false, false><<<grid, kQT, kQuantSmem, s>>>(A);
+    if (f46 && dual) k_quant_tiles<true, true><<<grid, kQT, quant_smem<true>(), s>>>(A);
+    else if (f46) k_quant_tiles<true, false><<<grid, kQT, quant_smem<false>(), s>>>(A);
+    else if (dual) k_quant_tiles<false, true><<<grid, kQT, quant_smem<true>(), s>>>(A);
+    else k_quant_tiles<false, false><<<grid, kQT, quant_smem<false>(), s>>>(A);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   return cudaSuccess;
