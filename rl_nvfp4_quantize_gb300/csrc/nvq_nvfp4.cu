@@ -120,9 +120,10 @@ cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, floa
 //                    results are staged and written as contiguous runs of the
 //                    transposed [in, out/2] layout.
 // Inside a swizzled box, 16-byte chunk c of row r sits at chunk c ^ (r & 7).
-#ifndef NVQ_QT_MINB
-#define NVQ_QT_MINB 2
-#endif
+// CTAs per SM: the dual kernel keeps two (128 registers; at three it spills
+// and runs 29 % slower), the rowwise-only kernel three (64 registers; 4 %
+// faster than two).
+constexpr int kQtMinbDual = 2, kQtMinbRow = 3;
 constexpr int kTR = 64, kTC = 256, kQT = 256;
 constexpr int kBoxC = 64;                       // box columns (128 bytes)
 constexpr int kBoxBytes = kTR * kBoxC * 2;      // 8 KiB
@@ -161,7 +162,7 @@ struct QuantTileArgs {  // aligned as CUtensorMap requires
 };
 
 template <bool F46, bool DUAL>
-__global__ void __launch_bounds__(kQT, NVQ_QT_MINB) k_quant_tiles(const __grid_constant__ QuantTileArgs A) {
+__global__ void __launch_bounds__(kQT, DUAL ? kQtMinbDual : kQtMinbRow) k_quant_tiles(const __grid_constant__ QuantTileArgs A) {
   // The kernel has no static shared memory, so the dynamic block starts at
   // the (1 KiB aligned) base of the CTA's window, as the swizzled TMA boxes
   // require; a misaligned base is reported instead of used.
@@ -446,7 +447,8 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
   A.sl_row = tiled_scale_bytes(rows, cols);
   A.sl_col = tiled_scale_bytes(cols, rows);
   A.col32 = (reinterpret_cast<uintptr_t>(codes_col) & 31) == 0;
-  const int full_grid = di->sms * NVQ_QT_MINB;
+  const bool dual = codes_col != nullptr;
+  const int full_grid = di->sms * (dual ? kQtMinbDual : kQtMinbRow);
   // Slices per launch: with the look-ahead amax every launch quantises one
   // chunk while reducing the amax of the next, so each launch must see its
   // chunk's amax complete.  A chunk covers about 40 waves of tiles, so the
@@ -472,7 +474,6 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
     cudaError_t err = launch_amax(w, chunk, (int64_t)rows * cols, amax, s);
     if (err != cudaSuccess) return err;
   }
-  const bool dual = codes_col != nullptr;
   cudaError_t err;
   if (f46 && dual) err = set_quant_smem<true, true>();
   else if (f46) err = set_quant_smem<true, false>();
