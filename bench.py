@@ -452,6 +452,7 @@ def main():
             e["dram_over_algorithmic"] = round(dram / b, 3)
         breakdown[n] = e
     st = int(wl.status.item())
+    n_routed = int(wl.nhit.item())  # of the timed steps' router (the context reuses the buffer)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -481,7 +482,7 @@ def main():
         "config": {"workload": WORKLOAD, "gate_up": list(GATE_UP), "down": list(DOWN),
                    "activations": [list(a) for a in ACTS], "router": [TOKENS, TOPK, "zipf1.1"],
                    "four_over_six": True, "l2": "inputs larger than L2 (gate_up 12.9 GB)",
-                   "routed_experts": int(wl.nhit.item()), "step_bytes": step_bytes,
+                   "routed_experts": n_routed, "step_bytes": step_bytes,
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "traffic": traffic,
