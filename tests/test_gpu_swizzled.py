@@ -84,7 +84,7 @@ def test_fp4_gemm_reads_the_swizzled_scales(nvq, oracle_mod):
         y = torch._scaled_mm(qx["codes"].view(fp4), qw["codes"][0].view(fp4).t(),
                              qx["scales"].view(fp8), qw["scales"][0].view(fp8),
                              out_dtype=torch.bfloat16)
-    except (RuntimeError, TypeError) as e:  # no NVFP4 GEMM in this build
+    except (RuntimeError, TypeError) as e:  # a torch without the block-scaled NVFP4 GEMM
         pytest.skip("torch._scaled_mm has no NVFP4 path here: %s" % str(e).splitlines()[0])
     torch.cuda.synchronize()
     ox = oracle_mod.act_quantize_per_token(u16(x), four_over_six=True)
