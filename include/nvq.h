@@ -18,7 +18,8 @@
  *    between calls (only per-device setup flags of its kernels, set once,
  *    atomically) and never synchronises the host.  Bulk buffers (bf16
  *    inputs and outputs, codes, scales, absmax) must be 16-byte aligned
- *    (32-byte where a call says so); FP32 and int32 arrays 4-byte aligned.
+ *    (32-byte, or only 4-byte, where a call says so); FP32 and int32 arrays
+ *    4-byte aligned.
  *  - bf16 tensors are passed as uint16_t bit patterns.  Shapes are int64.
  *    An expert stack is row-major [nexp, rows, cols] with cols contiguous;
  *    for an expert weight used as F.linear(x, W[e]) rows = out, cols = in
