@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -105,10 +106,12 @@ class Workload:
 
         def dual_launches(E, R, K):
             # one zeroing of amax, one amax pass over the first chunk, then one
-            # tile launch per chunk of slices (about 40 waves of 64 x 256 tiles
-            # over two CTAs per SM); checked against the ncu launch list
+            # tile launch per chunk of slices: sqrt(E * 5.6e7 / (R * K)) slices,
+            # at least 40 waves of 64 x 256 tiles over two CTAs per SM (the
+            # library's rule); checked against the ncu launch list
             per = -(-R // 64) * -(-K // 256)
-            chunk = min(E, max(1, -(-40 * 2 * sms // per)))
+            balanced = int(math.floor(math.sqrt(E * 5.6e7 / (R * K)) + 0.5))
+            chunk = min(E, max(1, balanced, -(-40 * 2 * sms // per)))
             return 2 + -(-E // chunk)
         L = []
         for name, w, q, n, E in (("nvfp4_quantize_dual[gate_up]", self.gu, self.q_gu, n_gu, GATE_UP[0]),

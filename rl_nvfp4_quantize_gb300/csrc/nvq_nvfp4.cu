@@ -9,6 +9,7 @@
 #include <cfloat>
 #include <algorithm>
 #include <cstdint>
+#include <cmath>
 #include <cstdlib>
 
 #include "nvq_common.cuh"
@@ -451,8 +452,13 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
   const int full_grid = di->sms * (dual ? kQtMinbDual : kQtMinbRow);
   // Slices per launch: with the look-ahead amax every launch quantises one
   // chunk while reducing the amax of the next, so each launch must see its
-  // chunk's amax complete.  A chunk covers about 40 waves of tiles, so the
-  // partial last wave of each launch costs little.
+  // chunk's amax complete.  Two costs set the chunk: every launch boundary
+  // (a partial last wave and the refill of the copy pipeline, about 16 us
+  // measured), and the separate amax pass over the first chunk (2 bytes per
+  // element at about 7 TB/s).  Their sum is smallest at
+  // chunk = sqrt(nexp * 16 us / amax time of one slice)
+  //       = sqrt(nexp * 5.6e7 / elements per slice),
+  // and a chunk is kept at 40 waves of tiles or more.
   // The look-ahead is used by the dual-layout kernel only (the rowwise kernel
   // is close to memory bound, where a separate reduction pass is as fast);
   // its reads are 32-byte vectors, so it also needs a 32-byte aligned stack.
@@ -461,7 +467,9 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
                          (reinterpret_cast<uintptr_t>(w) & 31) == 0;
   int64_t chunk = nexp;
   if (lookahead) {
-    chunk = std::max<int64_t>(1, (40ll * full_grid + per - 1) / per);
+    const double balanced = std::floor(std::sqrt((double)nexp * 5.6e7 / ((double)rows * cols)) + 0.5);
+    chunk = std::max<int64_t>((int64_t)balanced, (40ll * full_grid + per - 1) / per);
+    chunk = std::max<int64_t>(chunk, 1);
     // NVQ_QUANT_CHUNK (slices per launch) overrides the choice; the tests use
     // it to exercise the look-ahead on small stacks.
     if (const char* env = std::getenv("NVQ_QUANT_CHUNK")) {
