@@ -258,7 +258,9 @@ NVQ_API int nf4_dequant(const uint8_t* codes, const float* absmax, int64_t nexp,
  *   absmax  in   f32 [nexp, nblocks] (4-byte aligned; e.g. nf4_quantize's
  *                absmax with nblocks = rows * cols / 64)
  *   codes   out  u8 [nexp, nblocks] (E4M3 bytes)
- *   c1      out  f32 [nexp, ceil(nblocks / 256)]
+ *   c1      out  f32 [nexp, ceil(nblocks / 256)] (during the call it also
+ *                holds the slice's partial sums; the final values are the
+ *                block maxima)
  *   mean    out  f32 [nexp]
  *   status  out  nullable; NVQ_STATUS_NONFINITE for a non-finite mean or c1
  * nblocks <= 2^25 (NVQ_ERR_SHAPE otherwise).  nblocks == 0 writes mean = 0.
