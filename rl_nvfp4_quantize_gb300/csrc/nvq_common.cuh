@@ -438,16 +438,6 @@ struct FastDiv {
   uint32_t d, m, s;
   __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> s; }
 };
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-  uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
 
 // ---------------------------------------------------- TMA and mbarriers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -518,15 +508,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// 2-D tiled TMA store of one box from shared memory (x, y as above, both
-// non-negative); completion is tracked with bulk async groups.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y,
-                                             const void* smem_src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   map),
-               "r"(x), "r"(y), "r"(smem_u32(smem_src))
-               : "memory");
-}
 // 3-D tiled TMA store of one box (coordinates non-negative; parts of the box
 // outside the tensor are not written).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
