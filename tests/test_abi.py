@@ -184,3 +184,39 @@ def test_valid_call_without_gpu_reports_device(nvq):
     assert nvq.lib.nf4_dequant_routed(ok16, ok16, 4, 4, 64, ok16, 2, 2, ok16, ok16, ok16, P, P) == 5
     assert nvq.lib.nf4_absmax_nest(ok16, 2, 8, ok16, ok16, ok16, P, P) == 5
     assert nvq.lib.nf4_absmax_unnest(ok16, ok16, ok16, 2, 8, ok16, P) == 5
+
+
+_C_CONSUMER = r"""
+#include <stddef.h>
+#include "nvq.h"
+int main(void) {
+  /* validation paths only: no device work */
+  if (nvq_version() >> 16 != 1) return 1;
+  if (nvq_scale_bytes(128, 64, 0) != 128 * 4) return 2;
+  if (nf4_absmax_unnest(NULL, NULL, NULL, 2, 0, NULL, NULL) != NVQ_OK) return 3;
+  if (nvfp4_quantize(NULL, 1, 16, 24, 0, NULL, NULL, NULL, NULL, NULL, NULL) != NVQ_ERR_SHAPE)
+    return 4;
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(nvq, tmp_path):
+    """include/nvq.h compiles as C99 (-pedantic) and a C program links and
+    calls the library through it."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "consumer.c"
+    src.write_text(_C_CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(nvq.library_path)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, "-l:libnvq.so", "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, "C consumer failed with %d" % r.returncode
