@@ -91,7 +91,18 @@ lib = _load()
 # ---------------------------------------------------------------- helpers
 
 def _ptr(t):
-    return None if t is None else C.c_void_p(t.data_ptr())
+    """Address of a contiguous tensor on the current CUDA device (None: NULL).
+    Host tensors are refused here: the kernels would dereference a host
+    address."""
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise TypeError("expected a contiguous CUDA tensor, got %s (%s, contiguous=%s)"
+                        % (tuple(t.shape), t.device, t.is_contiguous()))
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError("tensor on %s, but the current device is cuda:%d"
+                         % (t.device, torch.cuda.current_device()))
+    return C.c_void_p(t.data_ptr())
 
 
 def _stream(stream=None):

@@ -220,3 +220,21 @@ def test_header_is_plain_c_and_links(nvq, tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, "C consumer failed with %d" % r.returncode
+
+
+def test_binding_refuses_host_tensors(nvq):
+    """Every tensor the binding hands to the library must be a contiguous CUDA
+    tensor; host tensors are refused before any call (no device needed)."""
+    import torch
+    codes = torch.zeros((2, 8), dtype=torch.uint8)
+    c1 = torch.zeros((2, 1), dtype=torch.float32)
+    mean = torch.zeros(2, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        nvq.nf4_absmax_unnest(codes, c1, mean)
+    with pytest.raises(TypeError):
+        nvq.nf4_absmax_nest(torch.ones((2, 8), dtype=torch.float32))
+    with pytest.raises(TypeError):
+        nvq.nvfp4_dequant(torch.zeros((1, 16, 8), dtype=torch.uint8),
+                          torch.zeros((1, 16, 1), dtype=torch.uint8), torch.ones(1))
+    with pytest.raises(TypeError):
+        nvq.nvfp4_quantize(torch.zeros((1, 16, 16), dtype=torch.bfloat16))
