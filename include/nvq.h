@@ -301,9 +301,10 @@ NVQ_API int nf4_dequant_routed(const uint8_t* codes, const float* absmax, int64_
 /*
  * nvq_nf4_codebook -- copies the 16 NF4 levels the kernels use (ascending,
  * level 7 = 0, levels 0 and 15 = -1 and +1) into `out` (HOST, 16 floats).
- * The levels are standard-normal quantiles, 7 negative, zero, 8 positive,
- * at probabilities evenly spaced from 1/2 to 31/32 on each side, normalised
- * to [-1, 1] (the construction behind NF4 in [P5] "The fix").
+ * They are the binary32 values of QLoRA's NF4 data type (the type behind
+ * quant_type "nf4" in [P5] "The fix"): standard-normal quantiles, 7
+ * negative, zero, 8 positive, at probabilities spaced evenly between the
+ * outer probability 0.9677083 and 1/2, normalised to [-1, 1].
  */
 NVQ_API int nvq_nf4_codebook(float* out);
 

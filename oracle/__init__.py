@@ -8,9 +8,9 @@ The arithmetic lives in ``nvq_oracle.c`` (plain C, one thread, binary32 with
 contraction off).  This module compiles it with gcc and wraps it for numpy
 arrays.  Every function cites the source passage it restates in the C file.
 
-Parity status: all functions are pinned by host tests; the NF4 level table is
-"parity unpinned" against third-party tables (it is derived here from the
-published normal-quantile construction).  The nested absmax follows the
+Parity status: all functions are pinned by host tests; the NF4 level table
+is pinned to the NF4 values printed in the QLoRA paper.  The nested absmax
+follows the
 published double quantisation with the readings stated in the C file; its
 equality with any third-party nested code (whose 8-bit table differs) is not
 claimed.

@@ -28,10 +28,10 @@
  *
  * Parity pins: every function here is pinned by the host tests against
  * something other than itself (library conversions, hand-computed blocks, the
- * worked example of [P1], closed forms, invariants, brute force).  One part
- * is "parity unpinned" against prior art: the NF4 level table is derived here
- * from the published normal-quantile construction, and its equality with any
- * third-party table is not claimed.
+ * worked example of [P1], closed forms, invariants, brute force, and the NF4
+ * values printed in the QLoRA paper's appendix).  The nested NF4 absmax
+ * follows the published double quantisation with the readings stated at
+ * it; its equality with a third-party nested code is not claimed.
  */
 #include <float.h>
 #include <math.h>
@@ -435,27 +435,45 @@ static double std_normal_quantile(double p)
 }
 
 /*
- * The 16 NF4 levels, ascending.  The sources name NF4 (the QLoRA data type)
- * but print no values ([P5] "The fix").  Reading taken from the QLoRA
- * construction: levels are quantiles of N(0,1), asymmetric so that zero is
- * exact -- 7 negative levels, 0, and 8 positive levels -- normalised into
- * [-1, 1].  Each half uses probabilities evenly spaced from 1/2 to
- * delta = 31/32, the centre of the outermost of 16 equal-probability bins:
- *   positive j = 1..8:  Phi^-1(1/2 + j (delta - 1/2) / 8) / Phi^-1(delta)
- *   negative j = 7..1: -Phi^-1(1/2 + j (delta - 1/2) / 7) / Phi^-1(delta)
- * computed in double and rounded once to binary32.
+ * The 16 NF4 levels, ascending.  The pages name NF4 (bitsandbytes'
+ * quant_type "nf4", [P5] "The fix") but print no values; NF4 is the 4-bit
+ * NormalFloat data type of QLoRA (Dettmers et al. 2023, "4-bit NormalFloat
+ * Quantization" and the NF4 value list in its appendix).  Construction, in
+ * that paper's order:
+ *   1. quantiles of N(0,1) at probabilities spaced evenly between the outer
+ *      probability delta and 1/2: eight on the positive side (9 points,
+ *      1/2 dropped) and seven on the negative side (8 points, 1/2 dropped),
+ *      so that zero is an exact level and the type is asymmetric;
+ *   2. the two sets joined with one zero and normalised by the largest
+ *      level into [-1, 1].
+ * delta is the published offset 0.9677083 (1 - (1/32 + 1/30)/2 to seven
+ * digits).  Precision, the reading that reproduces the published binary32
+ * values bit for bit: delta and the probabilities are binary32, stepped from
+ * both ends (p_i = delta + i*s for the first half, 1/2 - (n-1-i)*s for the
+ * rest, s = (1/2 - delta)/(n-1)); each quantile is computed in double and
+ * rounded once to binary32; the normalisation is one binary32 division.
  */
+static void nf4_probabilities(int n, float p[9])
+{
+    const float d = 0.9677083f, h = 0.5f;
+    const float s = (h - d) / (float)(n - 1);
+    for (int i = 0; i < n; i++) {
+        if (i < n / 2) p[i] = d + s * (float)i;
+        else p[i] = h - s * (float)(n - 1 - i);
+    }
+}
+
 ORACLE_API void oracle_nf4_codebook(float cb[16])
 {
-    const double delta = 31.0 / 32.0;
-    double top = std_normal_quantile(delta);
-    for (int j = 7; j >= 1; j--)
-        cb[7 - j] = (float)(-std_normal_quantile(0.5 + j * (delta - 0.5) / 7.0) / top);
-    cb[7] = 0.0f;
-    for (int j = 1; j <= 8; j++)
-        cb[7 + j] = (float)(std_normal_quantile(0.5 + j * (delta - 0.5) / 8.0) / top);
-    cb[0] = -1.0f;
-    cb[15] = 1.0f;
+    float pp[9], pn[9], q[16];
+    nf4_probabilities(9, pp);   /* pp[0] = delta ... pp[8] = 1/2 */
+    nf4_probabilities(8, pn);   /* pn[0] = delta ... pn[7] = 1/2 */
+    /* ascending: -Phi^-1(pn[0]) ... -Phi^-1(pn[6]), 0, Phi^-1(pp[7]) ... Phi^-1(pp[0]) */
+    for (int i = 0; i < 7; i++) q[i] = (float)(-std_normal_quantile((double)pn[i]));
+    q[7] = 0.0f;
+    for (int i = 0; i < 8; i++) q[8 + i] = (float)std_normal_quantile((double)pp[7 - i]);
+    const float top = q[15];
+    for (int i = 0; i < 16; i++) cb[i] = q[i] / top;
 }
 
 /*

@@ -1,13 +1,17 @@
 """Pins of the oracle's NF4 path and routed-expert union.
 
-The NF4 levels are re-derived with scipy's normal quantile function (a
-library routine independent of the oracle's bisection over erfc); the
+The NF4 levels are pinned to the published NF4 values of the QLoRA paper
+(tests/golden/nf4_levels_qlora.json) and re-derived with scipy's normal
+quantile function (independent of the oracle's bisection over erfc); the
 quantiser is checked against a brute-force nearest-level search; dequant
 against torch's bfloat16 cast of the FP32 products; the union against a
 Python set.  Source: "nf4moe -- QLoRA for a 743B Fused-MoE", "The fix:
 dequant-on-forward for routed experts" (NF4, blocksize 64, one-hot union of
 top_k_index).
 """
+import json
+from pathlib import Path
+
 import numpy as np
 import pytest
 import torch
@@ -16,14 +20,33 @@ from scipy.stats import norm
 from test_oracle_nvfp4 import bf16, bf16_to_float
 
 
-def test_codebook_against_scipy_quantiles(oracle_mod):
+GOLDEN = Path(__file__).parent / "golden" / "nf4_levels_qlora.json"
+
+
+def test_codebook_equals_published_nf4(oracle_mod):
+    """The oracle's levels are the published NF4 values (QLoRA appendix),
+    bit for bit as binary32 and to the printed precision."""
+    pub = np.array(json.loads(GOLDEN.read_text())["values"], np.float64)
     cb = oracle_mod.nf4_codebook()
-    delta = 31 / 32
-    top = norm.ppf(delta)
-    neg = [-norm.ppf(0.5 + j * (delta - 0.5) / 7) / top for j in range(7, 0, -1)]
-    pos = [norm.ppf(0.5 + j * (delta - 0.5) / 8) / top for j in range(1, 9)]
-    ref = np.array(neg + [0.0] + pos, np.float32)
-    assert np.array_equal(cb.view(np.uint32), ref.view(np.uint32))
+    assert np.array_equal(cb.view(np.uint32), pub.astype(np.float32).view(np.uint32))
+    assert np.all(np.abs(cb.astype(np.float64) - pub) < 5e-8)
+
+
+def test_codebook_is_the_normal_quantile_construction(oracle_mod):
+    """Independent restatement with scipy's normal quantile, everything in
+    double, at the outer probability 1 - (1/32 + 1/30)/2: every level agrees
+    within a few binary32 units (the binary32 probabilities of the published
+    values move them by less than 1e-6).  The same construction at the
+    outer probability 31/32 is far off, so a wrong offset cannot pass."""
+    def construct(delta):
+        top = norm.ppf(delta)
+        neg = [-norm.ppf(0.5 + j * (delta - 0.5) / 7) / top for j in range(7, 0, -1)]
+        pos = [norm.ppf(0.5 + j * (delta - 0.5) / 8) / top for j in range(1, 9)]
+        return np.array(neg + [0.0] + pos)
+
+    cb = oracle_mod.nf4_codebook().astype(np.float64)
+    assert np.max(np.abs(cb - construct(1 - (1 / 32 + 1 / 30) / 2))) < 1e-6
+    assert np.max(np.abs(cb - construct(31 / 32))) > 1e-3
 
 
 def test_codebook_structure(oracle_mod):
