@@ -116,8 +116,9 @@ def _check(fn: str, rc: int):
 
 
 def _bf16(t, name):
-    if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
-        raise TypeError("%s must be a contiguous CUDA bfloat16 tensor" % name)
+    """A bf16 input; its device is checked by _ptr, after the size checks."""
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous bfloat16 tensor" % name)
     return t
 
 
@@ -131,6 +132,34 @@ def _as3d(w):
 
 def _empty(shape, dtype, like):
     return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def _need(t, name, dtype, numel=None, shape=None, at_least=False):
+    """Refuses, before any call, a tensor the library would read or write
+    past its end or reinterpret: the C ABI sees only an address, so its size
+    and element type are checked here.  `numel` is the exact element count
+    the call touches (`at_least`: a lower bound); `shape`, when given, must
+    match exactly.  Returns t."""
+    if t is None:
+        return t
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if numel is not None:
+        n = t.numel()
+        if (n < numel) if at_least else (n != numel):
+            raise ValueError("%s must hold %s%d elements, got %d"
+                             % (name, "at least " if at_least else "", numel, n))
+    return t
+
+
+def _status(status):
+    return _need(status, "status", torch.int32, 1, at_least=True)
+
+
+def _scale_numel(E, R, K, swizzled):
+    return E * scale_bytes(R, K, True) if swizzled else E * R * (K // 16)
 
 
 # ---------------------------------------------------------------- NVFP4
@@ -164,8 +193,14 @@ def nvfp4_quantize(w, four_over_six=False, amax=None, status=None, stream=None, 
     scales = o.get("scales") if "scales" in o else _scales(E, R, K, swizzled_scales, w)
     am = amax if amax is not None else o.get("amax", _empty((E,), torch.float32, w))
     G = o.get("tensor_scale", _empty((E,), torch.float32, w))
+    if K % 16 == 0:
+        _need(codes, "codes", torch.uint8, E * R * (K // 2))
+        _need(scales, "scales", torch.uint8, _scale_numel(E, R, K, swizzled_scales))
+    _need(am, "amax", torch.float32, E)
+    _need(G, "tensor_scale", torch.float32, E)
     flags = ((FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
              | (FLAG_SCALES_SWIZZLED if swizzled_scales else 0))
+    _status(status)
     _check("nvfp4_quantize", lib.nvfp4_quantize(_ptr(w), E, R, K, flags, _ptr(codes), _ptr(scales),
                                                 _ptr(am), _ptr(G), _ptr(status), _stream(stream)))
     return dict(codes=codes, scales=scales, amax=am, tensor_scale=G)
@@ -185,19 +220,42 @@ def nvfp4_quantize_dual(w, four_over_six=True, amax=None, status=None, stream=No
     sc = o.get("scales_col") if "scales_col" in o else _scales(E, K, R, swizzled_scales, w)
     am = amax if amax is not None else o.get("amax", _empty((E,), torch.float32, w))
     G = o.get("tensor_scale", _empty((E,), torch.float32, w))
+    if K % 16 == 0 and R % 16 == 0:
+        _need(cr, "codes_row", torch.uint8, E * R * (K // 2))
+        _need(sr, "scales_row", torch.uint8, _scale_numel(E, R, K, swizzled_scales))
+        _need(cc, "codes_col", torch.uint8, E * K * (R // 2))
+        _need(sc, "scales_col", torch.uint8, _scale_numel(E, K, R, swizzled_scales))
+    _need(am, "amax", torch.float32, E)
+    _need(G, "tensor_scale", torch.float32, E)
     flags = ((FLAG_4OVER6 if four_over_six else 0) | (FLAG_AMAX_GIVEN if amax is not None else 0)
              | (FLAG_SCALES_SWIZZLED if swizzled_scales else 0))
+    _status(status)
     _check("nvfp4_quantize_dual",
            lib.nvfp4_quantize_dual(_ptr(w), E, R, K, flags, _ptr(cr), _ptr(sr), _ptr(cc), _ptr(sc),
                                    _ptr(am), _ptr(G), _ptr(status), _stream(stream)))
     return dict(codes_row=cr, scales_row=sr, codes_col=cc, scales_col=sc, amax=am, tensor_scale=G)
 
 
-def nvfp4_dequant(codes, scales, tensor_scale, stream=None, out=None):
-    """DQ(Q(w)) in the layout of the codes: bf16 [nexp, rows, cols]."""
+def _dequant_inputs(codes, scales, tensor_scale):
+    """Shapes of the rowwise copy a dequant call reads.  The scales must be
+    in the linear layout [nexp, rows, cols/16]: a tiled (swizzled_scales)
+    buffer is refused rather than decoded as linear."""
+    _need(codes, "codes", torch.uint8)
+    if codes.dim() != 3:
+        raise ValueError("codes must be [nexp, rows, cols/2]")
     E, R, K2 = codes.shape
     K = K2 * 2
+    if K % 16 == 0:
+        _need(scales, "scales", torch.uint8, shape=(E, R, K // 16))
+    _need(tensor_scale, "tensor_scale", torch.float32, E)
+    return E, R, K
+
+
+def nvfp4_dequant(codes, scales, tensor_scale, stream=None, out=None):
+    """DQ(Q(w)) in the layout of the codes: bf16 [nexp, rows, cols]."""
+    E, R, K = _dequant_inputs(codes, scales, tensor_scale)
     dst = out if out is not None else _empty((E, R, K), torch.bfloat16, codes)
+    _need(dst, "out", torch.bfloat16, E * R * K)
     _check("nvfp4_dequant", lib.nvfp4_dequant(_ptr(codes), _ptr(scales), _ptr(tensor_scale), E, R, K,
                                               _ptr(dst), _stream(stream)))
     return dst
@@ -205,9 +263,9 @@ def nvfp4_dequant(codes, scales, tensor_scale, stream=None, out=None):
 
 def nvfp4_dequant_t(codes_row, scales_row, tensor_scale, stream=None, out=None):
     """DQ(Q(w)) of the rowwise copy, transposed: bf16 [nexp, in, out]."""
-    E, R, K2 = codes_row.shape
-    K = K2 * 2
+    E, R, K = _dequant_inputs(codes_row, scales_row, tensor_scale)
     dst = out if out is not None else _empty((E, K, R), torch.bfloat16, codes_row)
+    _need(dst, "out", torch.bfloat16, E * K * R)
     _check("nvfp4_dequant_t",
            lib.nvfp4_dequant_t(_ptr(codes_row), _ptr(scales_row), _ptr(tensor_scale), E, R, K,
                                _ptr(dst), _stream(stream)))
@@ -231,6 +289,11 @@ def act_quantize_per_token(x, four_over_six=True, status=None, stream=None, out=
     else:
         scales = _empty((T, H // 16), torch.uint8, x)
     ts = o.get("token_scale", _empty((T,), torch.float32, x))
+    if H % 16 == 0:
+        _need(codes, "codes", torch.uint8, T * (H // 2))
+        _need(scales, "scales", torch.uint8, _scale_numel(1, T, H, swizzled_scales))
+    _need(ts, "token_scale", torch.float32, T)
+    _status(status)
     flags = (FLAG_4OVER6 if four_over_six else 0) | (FLAG_SCALES_SWIZZLED if swizzled_scales else 0)
     _check("act_quantize_per_token",
            lib.act_quantize_per_token(_ptr(x), T, H, flags, _ptr(codes), _ptr(scales), _ptr(ts),
@@ -247,15 +310,30 @@ def nf4_quantize(w, status=None, stream=None, out=None):
     o = out or {}
     codes = o.get("codes", _empty((E, R, K // 2), torch.uint8, w))
     absmax = o.get("absmax", _empty((E, R, K // 64), torch.float32, w))
+    if K % 64 == 0:
+        _need(codes, "codes", torch.uint8, E * R * (K // 2))
+        _need(absmax, "absmax", torch.float32, E * R * (K // 64))
+    _status(status)
     _check("nf4_quantize", lib.nf4_quantize(_ptr(w), E, R, K, _ptr(codes), _ptr(absmax),
                                             _ptr(status), _stream(stream)))
     return dict(codes=codes, absmax=absmax)
 
 
-def nf4_dequant(codes, absmax, stream=None, out=None):
+def _nf4_inputs(codes, absmax):
+    _need(codes, "codes", torch.uint8)
+    if codes.dim() != 3:
+        raise ValueError("codes must be [nexp, rows, cols/2]")
     E, R, K2 = codes.shape
     K = K2 * 2
+    if K % 64 == 0:
+        _need(absmax, "absmax", torch.float32, E * R * (K // 64))
+    return E, R, K
+
+
+def nf4_dequant(codes, absmax, stream=None, out=None):
+    E, R, K = _nf4_inputs(codes, absmax)
     dst = out if out is not None else _empty((E, R, K), torch.bfloat16, codes)
+    _need(dst, "out", torch.bfloat16, E * R * K)
     _check("nf4_dequant", lib.nf4_dequant(_ptr(codes), _ptr(absmax), E, R, K, _ptr(dst),
                                           _stream(stream)))
     return dst
@@ -273,6 +351,10 @@ def nf4_absmax_nest(absmax, status=None, stream=None, out=None):
     codes = o.get("codes", _empty((E, n), torch.uint8, a))
     c1 = o.get("c1", _empty((E, (n + 255) // 256), torch.float32, a))
     mean = o.get("mean", _empty((E,), torch.float32, a))
+    _need(codes, "codes", torch.uint8, E * n)
+    _need(c1, "c1", torch.float32, E * ((n + 255) // 256))
+    _need(mean, "mean", torch.float32, E)
+    _status(status)
     _check("nf4_absmax_nest", lib.nf4_absmax_nest(_ptr(a), E, n, _ptr(codes), _ptr(c1), _ptr(mean),
                                                   _ptr(status), _stream(stream)))
     return dict(codes=codes, c1=c1, mean=mean)
@@ -280,9 +362,13 @@ def nf4_absmax_nest(absmax, status=None, stream=None, out=None):
 
 def nf4_absmax_unnest(codes, c1, mean, shape=None, stream=None, out=None):
     """FP32 absmax decoded from the nested form, [nexp, n] (or `shape`)."""
+    _need(codes, "codes", torch.uint8)
     E = codes.shape[0]
     n = codes.numel() // E if E else 0
+    _need(c1, "c1", torch.float32, E * ((n + 255) // 256))
+    _need(mean, "mean", torch.float32, E)
     dst = out if out is not None else _empty((E, n), torch.float32, codes)
+    _need(dst, "out", torch.float32, E * n)
     _check("nf4_absmax_unnest", lib.nf4_absmax_unnest(_ptr(codes), _ptr(c1), _ptr(mean), E, n,
                                                       _ptr(dst), _stream(stream)))
     return dst.view(shape) if shape is not None else dst
@@ -293,15 +379,18 @@ def nf4_dequant_routed(codes, absmax, topk_idx, dst=None, status=None, stream=No
     """Dequantises only the experts present in topk_idx [T, k] (int32) into
     dst [nexp, rows, cols]; returns (dst, hit_list, n_hit), both device
     tensors -- nothing is synchronised to the host."""
-    E, R, K2 = codes.shape
-    K = K2 * 2
-    if topk_idx.dtype != torch.int32 or not topk_idx.is_contiguous():
-        raise TypeError("topk_idx must be a contiguous int32 tensor")
+    E, R, K = _nf4_inputs(codes, absmax)
+    if topk_idx.dtype != torch.int32 or not topk_idx.is_contiguous() or topk_idx.dim() != 2:
+        raise TypeError("topk_idx must be a contiguous int32 tensor [T, k]")
     T, k = topk_idx.shape
     if dst is None:
         dst = _empty((E, R, K), torch.bfloat16, codes)
     hl = hit_list if hit_list is not None else _empty((E,), torch.int32, codes)
     nh = n_hit if n_hit is not None else _empty((1,), torch.int32, codes)
+    _need(dst, "dst", torch.bfloat16, E * R * K)
+    _need(hl, "hit_list", torch.int32, E)
+    _need(nh, "n_hit", torch.int32, 1, at_least=True)
+    _status(status)
     _check("nf4_dequant_routed",
            lib.nf4_dequant_routed(_ptr(codes), _ptr(absmax), E, R, K, _ptr(topk_idx), T, k,
                                   _ptr(dst), _ptr(hl), _ptr(nh), _ptr(status), _stream(stream)))
@@ -340,11 +429,15 @@ def nvfp4_dgrad(dy, counts, codes, scales, tensor_scale, status=None, stream=Non
     tokens per expert (host sequence); codes/scales/tensor_scale: the
     rowwise NVFP4 copy of the [nexp, out_dim, in_dim] stack.  Returns FP32
     dX [T, in_dim]."""
-    E, R, K2 = codes.shape
-    K = K2 * 2
+    E, R, K = _dequant_inputs(codes, scales, tensor_scale)
+    if len(counts) != E:
+        raise ValueError("counts must give one token count per expert (%d)" % E)
     cnt = (C.c_int64 * E)(*[int(c) for c in counts])
     T = sum(int(c) for c in counts)
+    _need(dy, "dy", torch.bfloat16, shape=(T, R))
     dst = out if out is not None else _empty((T, K), torch.float32, codes)
+    _need(dst, "out", torch.float32, shape=(T, K))
+    _status(status)
     _check("nvfp4_dgrad", lib.nvfp4_dgrad(_ptr(_bf16(dy, "dy")), C.cast(cnt, C.c_void_p), E, R, K,
                                           _ptr(codes),
                                           _ptr(scales), _ptr(tensor_scale), _ptr(dst),
@@ -357,11 +450,15 @@ def nf4_routed_linear(x, counts, codes, absmax, status=None, stream=None, out=No
     nf4_routed_linear in nvq.h).  x bf16 [T, in_dim] grouped by expert;
     counts: tokens per expert (host sequence); codes/absmax: the NF4 copy of
     the [nexp, out_dim, in_dim] stack.  Returns bf16 Y [T, out_dim]."""
-    E, R, K2 = codes.shape
-    K = K2 * 2
+    E, R, K = _nf4_inputs(codes, absmax)
+    if len(counts) != E:
+        raise ValueError("counts must give one token count per expert (%d)" % E)
     cnt = (C.c_int64 * E)(*[int(c) for c in counts])
     T = sum(int(c) for c in counts)
+    _need(x, "x", torch.bfloat16, shape=(T, K))
     dst = out if out is not None else _empty((T, R), torch.bfloat16, codes)
+    _need(dst, "out", torch.bfloat16, shape=(T, R))
+    _status(status)
     _check("nf4_routed_linear", lib.nf4_routed_linear(_ptr(_bf16(x, "x")), C.cast(cnt, C.c_void_p),
                                                       E, R, K, _ptr(codes), _ptr(absmax), _ptr(dst),
                                                       _ptr(status), _stream(stream)))
@@ -399,6 +496,15 @@ def mxfp8_quantize(w, columnwise=False, swizzled_scales=False, status=None, stre
     if columnwise:
         cc = o.get("codes_col", _empty((E, K, R), torch.uint8, w))
         sco = o.get("scales_col") if "scales_col" in o else sc(K, R)
+    if K % 32 == 0:
+        def sc_numel(rows, cols):
+            return E * (mx_scale_bytes(rows, cols, True) if swizzled_scales else rows * (cols // 32))
+        _need(cr, "codes_row", torch.uint8, E * R * K)
+        _need(sr, "scales_row", torch.uint8, sc_numel(R, K))
+        if columnwise and R % 32 == 0:
+            _need(cc, "codes_col", torch.uint8, E * K * R)
+            _need(sco, "scales_col", torch.uint8, sc_numel(K, R))
+    _status(status)
     flags = FLAG_SCALES_SWIZZLED if swizzled_scales else 0
     _check("mxfp8_quantize", lib.mxfp8_quantize(_ptr(w), E, R, K, flags, _ptr(cr), _ptr(sr), _ptr(cc),
                                                 _ptr(sco), _ptr(status), _stream(stream)))
@@ -411,7 +517,10 @@ def mxfp8_quantize(w, columnwise=False, swizzled_scales=False, status=None, stre
 def mxfp8_dequant(codes, scales, stream=None, out=None):
     """bf16 of MXFP8 codes (any shape whose last dimension holds whole blocks
     of 32) with their linear scales."""
+    _need(codes, "codes", torch.uint8)
+    _need(scales, "scales", torch.uint8, codes.numel() // 32)
     dst = out if out is not None else _empty(tuple(codes.shape), torch.bfloat16, codes)
+    _need(dst, "out", torch.bfloat16, codes.numel())
     _check("mxfp8_dequant", lib.mxfp8_dequant(_ptr(codes), _ptr(scales), codes.numel(), _ptr(dst),
                                               _stream(stream)))
     return dst

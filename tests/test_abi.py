@@ -238,3 +238,72 @@ def test_binding_refuses_host_tensors(nvq):
                           torch.zeros((1, 16, 1), dtype=torch.uint8), torch.ones(1))
     with pytest.raises(TypeError):
         nvq.nvfp4_quantize(torch.zeros((1, 16, 16), dtype=torch.bfloat16))
+
+
+def test_binding_refuses_mis_sized_buffers(nvq):
+    """The C ABI sees addresses only, so the binding checks the element type
+    and size of every buffer a call touches and raises before the call: a
+    short or mistyped out= buffer, scales, tensor_scale or absmax would
+    otherwise be read or written past its end on the GPU.  Host tensors of
+    the right size reach the host-tensor check instead (TypeError)."""
+    import torch
+    u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+    w = torch.zeros((2, 32, 64), dtype=bf)
+    # nvfp4_quantize(_dual): short codes / scales / amax / tensor_scale
+    for bad in (dict(codes=torch.zeros((2, 32, 31), dtype=u8)),
+                dict(scales=torch.zeros((2, 32, 3), dtype=u8)),
+                dict(tensor_scale=torch.zeros(1, dtype=f32)),
+                dict(amax=torch.zeros(2, dtype=torch.float64))):
+        with pytest.raises((ValueError, TypeError)) as ei:
+            nvq.nvfp4_quantize(w, out=bad)
+        assert "expected a contiguous CUDA tensor" not in str(ei.value)
+    with pytest.raises(ValueError):
+        nvq.nvfp4_quantize_dual(w, out=dict(codes_col=torch.zeros((2, 64, 15), dtype=u8)))
+    with pytest.raises(ValueError):
+        nvq.nvfp4_quantize_dual(w, out=dict(scales_col=torch.zeros((2, 64, 1), dtype=u8)))
+    with pytest.raises(ValueError):  # tiled scales need nvq_scale_bytes bytes per slice
+        nvq.nvfp4_quantize(w, swizzled_scales=True, out=dict(scales=torch.zeros((2, 32, 4), dtype=u8)))
+    # dequant calls: undersized scales / tensor_scale / out, and tiled scales
+    codes = torch.zeros((2, 32, 32), dtype=u8)
+    scales = torch.zeros((2, 32, 4), dtype=u8)
+    G = torch.ones(2, dtype=f32)
+    with pytest.raises(ValueError):
+        nvq.nvfp4_dequant(codes, scales[:, :16], G)
+    with pytest.raises(ValueError):
+        nvq.nvfp4_dequant(codes, scales, G[:1])
+    with pytest.raises(ValueError):
+        nvq.nvfp4_dequant_t(codes, scales, G, out=torch.zeros((2, 64, 31), dtype=bf))
+    with pytest.raises(ValueError):
+        nvq.nvfp4_dequant(codes, torch.zeros((2, nvq.scale_bytes(32, 64, True)), dtype=u8), G)
+    with pytest.raises(TypeError):  # right sizes: stopped by the host-tensor check
+        nvq.nvfp4_dequant(codes, scales, G)
+    # activations
+    x = torch.zeros((8, 64), dtype=bf)
+    with pytest.raises(ValueError):
+        nvq.act_quantize_per_token(x, out=dict(token_scale=torch.zeros(7, dtype=f32)))
+    # NF4: absmax and out
+    c4 = torch.zeros((2, 4, 64), dtype=u8)
+    with pytest.raises(ValueError):
+        nvq.nf4_dequant(c4, torch.zeros((2, 4, 1), dtype=f32))
+    with pytest.raises(ValueError):
+        nvq.nf4_quantize(torch.zeros((2, 4, 128), dtype=bf),
+                         out=dict(absmax=torch.zeros((2, 4, 1), dtype=f32)))
+    with pytest.raises(ValueError):
+        nvq.nf4_dequant_routed(c4, torch.zeros((2, 4, 2), dtype=f32),
+                               torch.zeros((3, 2), dtype=torch.int32),
+                               hit_list=torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        nvq.nf4_absmax_unnest(torch.zeros((2, 300), dtype=u8), torch.zeros((2, 1), dtype=f32),
+                              torch.zeros(2, dtype=f32))
+    # status words are int32
+    with pytest.raises(TypeError):
+        nvq.nvfp4_quantize(w, status=torch.zeros(1, dtype=torch.int64))
+    # GEMMs: dy / x must match the token counts and the stack
+    with pytest.raises(ValueError):
+        nvq.nvfp4_dgrad(torch.zeros((5, 32), dtype=bf), [2, 2], codes, scales, G)
+    with pytest.raises(ValueError):
+        nvq.nf4_routed_linear(torch.zeros((4, 100), dtype=bf), [2, 2], c4,
+                              torch.zeros((2, 4, 2), dtype=f32))
+    # MXFP8
+    with pytest.raises(ValueError):
+        nvq.mxfp8_dequant(torch.zeros((4, 64), dtype=u8), torch.zeros(7, dtype=u8))
