@@ -102,17 +102,11 @@ class Workload:
         import rl_nvfp4_quantize_gb300 as nvq
         n_gu = GATE_UP[0] * GATE_UP[1] * GATE_UP[2]
         n_dn = DOWN[0] * DOWN[1] * DOWN[2]
-        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
 
         def dual_launches(E, R, K):
-            # one zeroing of amax, one amax pass over the first chunk, then one
-            # tile launch per chunk of slices: sqrt(E * 5.6e7 / (R * K)) slices,
-            # at least 40 waves of 64 x 256 tiles over two CTAs per SM (the
-            # library's rule); checked against the ncu launch list
-            per = -(-R // 64) * -(-K // 256)
-            balanced = int(math.floor(math.sqrt(E * 5.6e7 / (R * K)) + 0.5))
-            chunk = min(E, max(1, balanced, -(-40 * 2 * sms // per)))
-            return 2 + -(-E // chunk)
+            # zeroing of amax and the arrival counters, the single pass over
+            # the stack, the tensor scales
+            return 3
         L = []
         for name, w, q, n, E in (("nvfp4_quantize_dual[gate_up]", self.gu, self.q_gu, n_gu, GATE_UP[0]),
                                  ("nvfp4_quantize_dual[down]", self.dn, self.q_dn, n_dn, DOWN[0])):

@@ -145,9 +145,19 @@ NVQ_API const char* nvq_status_string(int code);
  *            NVQ_SCALES_SWIZZLED: nexp slices of nvq_scale_bytes(rows, cols,
  *            NVQ_SCALES_SWIZZLED) bytes in the tiled layout)
  *   amax     in/out f32 [nexp]  (input iff NVQ_AMAX_GIVEN; empty slices give 0)
- *   tensor_scale out f32 [nexp] G_e
+ *   tensor_scale out f32 [nexp] G_e.  Until the call's last kernel writes
+ *            G_e, the call uses this buffer as its per-slice work counters,
+ *            so it must not be read before the call completes.
  *   status   out  device int, nullable (with NVQ_AMAX_GIVEN the input is not
  *            scanned, so only a non-finite given amax is reported)
+ *
+ * The stack is read from HBM once: the kernel reduces each slice's amax
+ * from tiles it loads a little more than one slice ahead of the tiles it
+ * quantises, which are then read again from L2.  The quantising kernel is
+ * a cooperative launch (all its CTAs resident at once), because a CTA that
+ * starts a slice waits, bounded, for the amax of that slice; if a wait
+ * gives up, NVQ_STATUS_TIMEOUT is set in *status and the outputs are
+ * unspecified.
  */
 NVQ_API int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols,
                    unsigned flags, uint8_t* codes, uint8_t* scales, float* amax,
@@ -425,6 +435,32 @@ NVQ_API int nvq_debug_convert(int kind, const void* in, void* out, int64_t n, nv
  *   status     device int, required
  */
 NVQ_API int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream);
+
+/*
+ * nvq_debug_count_timeout -- exercises the bounded wait of nvfp4_quantize
+ * and nvfp4_quantize_dual for a slice's amax: one thread polls the word at
+ * `counter` (device u32, which the caller leaves with bit 31 clear and
+ * nothing writes) for the finished mark, bit 31, for at most `max_polls`
+ * polls, then ORs NVQ_STATUS_TIMEOUT into *status and returns.  Nothing is
+ * left running, so the device stays usable.
+ *   max_polls  1 .. 65536 (larger values return NVQ_ERR_SHAPE)
+ *   counter    device u32, 4-byte aligned, required
+ *   status     device int, required
+ */
+NVQ_API int nvq_debug_count_timeout(uint32_t max_polls, const uint32_t* counter, int* status,
+                                    nvq_stream_t stream);
+
+/*
+ * nvq_debug_set_quant_lead -- how far beyond one slice the single-pass amax
+ * of nvfp4_quantize and nvfp4_quantize_dual reads ahead of the tiles being
+ * quantised, in waves of the kernel's grid (default 2, also the least that
+ * keeps every wait of the kernel acyclic).  Outputs do not depend on it;
+ * at 2 the slices' amax complete shortly before they are needed.
+ * Process-wide setting for tests and tuning, read at each call.
+ *   waves   2 .. 8 (other values return NVQ_ERR_SHAPE and change nothing)
+ * Host only; returns NVQ_OK.
+ */
+NVQ_API int nvq_debug_set_quant_lead(int waves);
 
 #ifdef __cplusplus
 }

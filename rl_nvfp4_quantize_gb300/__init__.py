@@ -27,7 +27,8 @@ __all__ = [
     "act_quantize_per_token", "nf4_quantize", "nf4_dequant", "nf4_dequant_routed", "nf4_routed_linear",
     "nf4_absmax_nest", "nf4_absmax_unnest",
     "mxfp8_quantize", "mxfp8_dequant", "mx_scale_bytes",
-    "nf4_codebook", "scale_bytes", "debug_convert", "debug_wait_timeout", "lib", "library_path",
+    "nf4_codebook", "scale_bytes", "debug_convert", "debug_wait_timeout", "debug_set_quant_lead",
+    "debug_count_timeout", "lib", "library_path",
 ]
 
 FLAG_4OVER6 = 1
@@ -69,6 +70,8 @@ def _load():
         "nvq_nf4_codebook": ([P], i32),
         "nvq_debug_convert": ([i32, P, P, i64, P], i32),
         "nvq_debug_wait_timeout": ([u32, P, P], i32),
+        "nvq_debug_set_quant_lead": ([i32], i32),
+        "nvq_debug_count_timeout": ([u32, P, P, P], i32),
         "nvfp4_dgrad": ([P, P, i64, i64, i64, P, P, P, P, P, P], i32),
         "nf4_routed_linear": ([P, P, i64, i64, i64, P, P, P, P, P], i32),
         "mxfp8_quantize": ([P, i64, i64, i64, u32, P, P, P, P, P, P], i32),
@@ -421,6 +424,22 @@ def debug_wait_timeout(max_tries: int, status, stream=None):
     """Runs the bounded-wait probe (see nvq_debug_wait_timeout): ORs
     STATUS_TIMEOUT into the device int `status`."""
     _check("nvq_debug_wait_timeout", lib.nvq_debug_wait_timeout(max_tries, _ptr(status), _stream(stream)))
+
+
+def debug_count_timeout(max_polls: int, counter, status, stream=None):
+    """Runs the quantisers' slice-amax wait on `counter` (a device int32 the
+    caller leaves non-negative; see nvq_debug_count_timeout): ORs
+    STATUS_TIMEOUT into the device int `status`."""
+    _need(counter, "counter", torch.int32, 1, at_least=True)
+    _need(status, "status", torch.int32, 1, at_least=True)
+    _check("nvq_debug_count_timeout",
+           lib.nvq_debug_count_timeout(max_polls, _ptr(counter), _ptr(status), _stream(stream)))
+
+
+def debug_set_quant_lead(waves: int):
+    """Sets the quantisers' look-ahead lead beyond one slice, in grid waves
+    (see nvq_debug_set_quant_lead); outputs do not depend on it."""
+    _check("nvq_debug_set_quant_lead", lib.nvq_debug_set_quant_lead(int(waves)))
 
 
 def nvfp4_dgrad(dy, counts, codes, scales, tensor_scale, status=None, stream=None, out=None):

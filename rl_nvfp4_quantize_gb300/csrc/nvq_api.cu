@@ -166,6 +166,19 @@ cudaError_t launch_debug_wait_timeout(uint32_t max_tries, int* status, cudaStrea
   return cudaGetLastError();
 }
 
+// The quantisers' wait for a slice's finished word, on a word that the
+// caller left without the finished bit and nothing writes.
+__global__ void k_debug_count_timeout(uint32_t max_polls, const uint32_t* counter, int* status) {
+  uint32_t w;
+  if (threadIdx.x == 0 && !wait_done(counter, w, max_polls)) atomicOr(status, kStatusTimeout);
+}
+
+cudaError_t launch_debug_count_timeout(uint32_t max_polls, const uint32_t* counter, int* status,
+                                       cudaStream_t s) {
+  k_debug_count_timeout<<<1, 32, 0, s>>>(max_polls, counter, status);
+  return cudaGetLastError();
+}
+
 }  // namespace nvq
 
 // ---------------------------------------------------------------- the C ABI
@@ -260,8 +273,10 @@ int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols, 
   const bool f46 = flags & NVQ_4OVER6;
   const bool given = flags & NVQ_AMAX_GIVEN;
   const bool tiled = flags & NVQ_SCALES_SWIZZLED;
-  if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
-  if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
+  if (total == 0) {
+    if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
+    return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, status, s));
+  }
   if (tiled && (rc = zero_tiled_padding(scales, nexp, rows, cols, s))) return rc;
   return launch_result(nvq::launch_quant_tiles(w, nexp, (int)rows, (int)cols, f46, codes, scales,
                                                nullptr, nullptr, amax, tensor_scale, status,
@@ -292,8 +307,10 @@ int nvfp4_quantize_dual(const uint16_t* w, int64_t nexp, int64_t out, int64_t in
   const bool f46 = flags & NVQ_4OVER6;
   const bool given = flags & NVQ_AMAX_GIVEN;
   const bool tiled = flags & NVQ_SCALES_SWIZZLED;
-  if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
-  if (total == 0) return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, s));
+  if (total == 0) {
+    if (!given && (rc = launch_result(nvq::launch_zero_f32(amax, nexp, s)))) return rc;
+    return launch_result(nvq::launch_tensor_scales(amax, tensor_scale, nexp, f46, status, s));
+  }
   if (tiled && ((rc = zero_tiled_padding(scales_row, nexp, out, in, s)) ||
                 (rc = zero_tiled_padding(scales_col, nexp, in, out, s))))
     return rc;
@@ -580,6 +597,22 @@ int nvq_debug_wait_timeout(uint32_t max_tries, int* status, nvq_stream_t stream)
   int rc = device_check();
   if (rc) return rc;
   return launch_result(nvq::launch_debug_wait_timeout(max_tries, status, cs(stream)));
+}
+
+int nvq_debug_count_timeout(uint32_t max_polls, const uint32_t* counter, int* status,
+                            nvq_stream_t stream) {
+  if (max_polls == 0 || max_polls > 65536u) return NVQ_ERR_SHAPE;
+  if (!status || !counter) return NVQ_ERR_NULL;
+  if (!aligned(status, 4) || !aligned(counter, 4)) return NVQ_ERR_ALIGN;
+  int rc = device_check();
+  if (rc) return rc;
+  return launch_result(nvq::launch_debug_count_timeout(max_polls, counter, status, cs(stream)));
+}
+
+int nvq_debug_set_quant_lead(int waves) {
+  if (waves < 2 || waves > 8) return NVQ_ERR_SHAPE;
+  nvq::g_quant_lead_waves.store(waves, std::memory_order_relaxed);
+  return NVQ_OK;
 }
 
 }  // extern "C"

@@ -497,6 +497,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// Non-blocking: whether the phase of `bar` with the given parity has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Barrier `id` (1 .. 15) over the first `n` threads that reach it: a group
+// of warps synchronising without the rest of the CTA.
+__device__ __forceinline__ void named_barrier(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// named_barrier that also returns whether `pred` held for any of the n threads.
+__device__ __forceinline__ bool named_barrier_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // 2-D tiled TMA load of one box at element coordinates (x, y) into shared
 // memory, completing on `bar` (x * element size must be a multiple of 16).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
@@ -506,6 +539,73 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "%3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 eviction policies for the cache-hinted loads below: evict-first for
+// data read for the last time, evict-last for data that is read again soon.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 eviction policy.
+__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, int x,
+                                                 int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------ grid-wide arrival counts
+// Words shared by the CTAs of one co-resident grid.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Returns the old value; the release orders the thread's earlier memory
+// operations (and those ordered before them in its CTA) before the add.
+__device__ __forceinline__ uint32_t atom_add_release(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A per-slice word holding a finished result has its sign bit set.
+constexpr uint32_t kSliceDone = 0x80000000u;
+
+// Polls *p until its kSliceDone bit is set (the word is returned in `w`),
+// giving up after `max_polls` polls or kMaxWaitNs of wall-clock time,
+// whichever comes first.  Returns false on giving up.
+__device__ __forceinline__ bool wait_done(const uint32_t* p, uint32_t& w,
+                                          uint32_t max_polls = 1u << 24) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < max_polls; i++) {
+    w = ld_relaxed_u32(p);
+    if (w & kSliceDone) return true;
+    const uint64_t now = globaltimer_ns();
+    if (i == 0) t0 = now;
+    else if (now - t0 > kMaxWaitNs) return false;
+    __nanosleep(32);
+  }
+  return false;
 }
 
 // 3-D tiled TMA store of one box (coordinates non-negative; parts of the box
@@ -559,6 +659,17 @@ __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+
+// Streaming (evict-first) 8-, 4- and 1-byte stores.
+__device__ __forceinline__ void stg_stream_v2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void stg_stream_u32(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+__device__ __forceinline__ void stg_stream_u8(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(a) : "memory");
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {

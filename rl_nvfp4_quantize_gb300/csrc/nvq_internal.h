@@ -79,21 +79,19 @@ struct DevInfo {
 // Current device's properties, or nullptr when there is no usable device.
 const DevInfo* device_info();
 
-// Zeroes n floats (the amax accumulators) on the stream.
-cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s);
+// Zeroes n floats at p (and at q, when given) on the stream.
+cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q = nullptr);
 
-// tensor_scale[e] = amax[e] / (6 M) for every slice (empty-slice case).
-cudaError_t launch_tensor_scales(const float* amax, float* G, int64_t n, bool f46, cudaStream_t s);
+// tensor_scale[e] = amax[e] / (6 M) for every slice; status bit 0 for a
+// non-finite amax.
+cudaError_t launch_tensor_scales(const float* amax, float* G, int64_t n, bool f46, int* status,
+                                 cudaStream_t s);
 
-// amax[e] = max |w| over slice e (atomic max of FP32 bit patterns; amax
-// must be zeroed first).  Sets status bit 0 for non-finite results.
-cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, float* amax,
-                        cudaStream_t s);
+// Lead of the quantisers' look-ahead beyond one slice, in waves of the grid
+// (default 1; a debug hook sets it).
+extern std::atomic<int> g_quant_lead_waves;
 
-// Rowwise (and, with codes_col != nullptr, columnwise) NVFP4 of a stack.
-// With compute_amax the per-slice amax (zeroed by the caller) is reduced
-// here: the first chunk of slices by a reduction pass, every later chunk
-// inside the launch that quantises the chunk before it.
+
 // Bytes of a [rows, nblocks] matrix of block scales in the tensor-core tiled
 // layout: rows padded to a multiple of 128, blocks per row to a multiple of 4.
 inline int64_t tiled_bytes(int64_t rows, int64_t nblocks) {
@@ -102,6 +100,10 @@ inline int64_t tiled_bytes(int64_t rows, int64_t nblocks) {
 // The same for the NVFP4 scales of a [rows, cols] slice (16-element blocks).
 inline int64_t tiled_scale_bytes(int64_t rows, int64_t cols) { return tiled_bytes(rows, cols / 16); }
 
+// Rowwise (and, with codes_col != nullptr, columnwise) NVFP4 of a stack,
+// then tensor_scale from amax.  With compute_amax the per-slice amax is
+// reduced inside the same single pass over the stack (tensor_scale serves
+// as the look-ahead counters until it is written); otherwise amax is given.
 // With tiled, the block scales are written in the tensor-core tiled layout
 // (padding entries are the caller's to zero).
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
@@ -143,6 +145,8 @@ cudaError_t launch_mx_dequant(const uint8_t* codes, const uint8_t* scales, int64
 
 cudaError_t launch_debug_convert(int kind, const void* in, void* out, int64_t n, cudaStream_t s);
 cudaError_t launch_debug_wait_timeout(uint32_t max_tries, int* status, cudaStream_t s);
+cudaError_t launch_debug_count_timeout(uint32_t max_polls, const uint32_t* counter, int* status,
+                                       cudaStream_t s);
 // Experts per grouped-GEMM call (nvfp4_dgrad, nf4_routed_linear): their
 // token and tile offsets travel in the kernel's parameter block.
 constexpr int kGroupedMaxExperts = 256;

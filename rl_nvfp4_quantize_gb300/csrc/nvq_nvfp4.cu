@@ -10,110 +10,99 @@
 #include <algorithm>
 #include <cstdint>
 #include <cmath>
-#include <cstdlib>
+#include <atomic>
 
 #include "nvq_common.cuh"
 #include "nvq_internal.h"
 
 namespace nvq {
 
-// ------------------------------------------------------------------ amax
-constexpr int kAmaxThreads = 256;
-constexpr int kAmaxVec = 8;  // 16-byte vectors per thread per item
-constexpr int64_t kAmaxChunk = (int64_t)kAmaxThreads * kAmaxVec * 8;  // elements per item
-
-__global__ void k_zero_f32(float* p, int64_t n) {
+// ------------------------------------------------------- per-slice scales
+// Zeroes p[0, n) and, when q is given, q[0, n).
+__global__ void k_zero_f32(float* p, float* q, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
+       i += (int64_t)gridDim.x * blockDim.x) {
     p[i] = 0.0f;
-}
-
-// Each work item is one chunk of one slice.  The magnitude maximum is taken
-// on bf16 bit patterns (exact); the item's result is folded into amax[e]
-// with an atomic max on the FP32 bit pattern (ordered like the values for
-// non-negative floats, NaN above infinity).
-__global__ void __launch_bounds__(kAmaxThreads)
-    k_amax(const uint16_t* __restrict__ w, int64_t per_slice, FastDiv cps, uint32_t nitems,
-           float* __restrict__ amax) {
-  __shared__ uint32_t red[kAmaxThreads / 32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (uint32_t it = blockIdx.x; it < nitems; it += gridDim.x) {
-    const uint32_t e = cps.div(it);
-    const int64_t start = (int64_t)(it - e * cps.d) * kAmaxChunk;
-    const uint16_t* base = w + (int64_t)e * per_slice;
-    uint4 v[kAmaxVec];
-#pragma unroll
-    for (int u = 0; u < kAmaxVec; u++) {
-      const int64_t idx = start + ((int64_t)u * kAmaxThreads + threadIdx.x) * 8;
-      v[u] = (idx < per_slice) ? ldg_stream(base + idx) : make_uint4(0, 0, 0, 0);
-    }
-    uint32_t m = 0;
-#pragma unroll
-    for (int u = 0; u < kAmaxVec; u++) {
-      m = umaxmag2(m, v[u].x);
-      m = umaxmag2(m, v[u].y);
-      m = umaxmag2(m, v[u].z);
-      m = umaxmag2(m, v[u].w);
-    }
-    uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
-    mm = __reduce_max_sync(0xffffffffu, mm);
-    if (lane == 0) red[warp] = mm;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t r = red[0];
-#pragma unroll
-      for (int i = 1; i < kAmaxThreads / 32; i++) r = max(r, red[i]);
-      atomicMax(reinterpret_cast<unsigned int*>(amax + e), r);
-    }
-    __syncthreads();
+    if (q) q[i] = 0.0f;
   }
 }
 
-// G[e] from amax[e] alone (used when the slices are empty).
-__global__ void k_tensor_scales(const float* amax, float* G, int64_t n, float six_m) {
+// G[e] = amax[e] / (6 M) for every slice, the last step of a quantisation
+// call (it also replaces the look-ahead counts kept in G), and status bit 0
+// for a non-finite amax.
+__global__ void k_tensor_scales(const float* amax, float* G, int64_t n, float six_m, int* status) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     float g, e;
-    global_scales(amax[i], six_m, g, e);
+    const float am = amax[i];
+    global_scales(am, six_m, g, e);
     G[i] = g;
+    if (status && !isfinite(am)) atomicOr(status, kStatusNonFinite);
   }
 }
 
-cudaError_t launch_tensor_scales(const float* amax, float* G, int64_t n, bool f46, cudaStream_t s) {
+cudaError_t launch_tensor_scales(const float* amax, float* G, int64_t n, bool f46, int* status,
+                                 cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   int grid = (int)std::min<int64_t>((n + 255) / 256, 1024);
-  k_tensor_scales<<<grid, 256, 0, s>>>(amax, G, n, f46 ? 1536.0f : 2688.0f);
+  k_tensor_scales<<<grid, 256, 0, s>>>(amax, G, n, f46 ? 1536.0f : 2688.0f, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s) {
+// Lead of the quantisers' look-ahead beyond one slice, in waves of the grid
+// (see k_quant_tiles).  Process-wide; nvq_debug_set_quant_lead changes it.
+std::atomic<int> g_quant_lead_waves{2};
+
+cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q) {
   if (n <= 0) return cudaSuccess;
   int grid = (int)std::min<int64_t>((n + 255) / 256, 1024);
-  k_zero_f32<<<grid, 256, 0, s>>>(p, n);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, float* amax,
-                        cudaStream_t s) {
-  const DevInfo* di = device_info();
-  const int64_t cps = (per_slice + kAmaxChunk - 1) / kAmaxChunk;
-  const int64_t nitems = nexp * cps;
-  if (nitems == 0) return cudaSuccess;
-  if (nitems >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
-  FastDiv fd;
-  fd.d = (uint32_t)cps;
-  make_fastdiv(fd.d, &fd.m, &fd.s);
-  int grid = (int)std::min<int64_t>(nitems, (int64_t)di->sms * 8);
-  k_amax<<<grid, kAmaxThreads, 0, s>>>(w, per_slice, fd, (uint32_t)nitems, amax);
+  k_zero_f32<<<grid, 256, 0, s>>>(p, q, n);
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------- rowwise / dual tiles
-// A CTA of 256 threads walks tiles of 64 rows x 256 columns of one expert
-// slice (persistent grid-stride loop).  One thread loads each tile with four
-// TMA box copies (64 x 64 bf16, 128-byte swizzle) into one of two shared
-// stages; the copy of the next tile runs while the current one is quantised.
-// From the staged tile:
+// One co-resident grid (cooperative launch), one CTA per SM, walks the
+// tiles of the whole stack -- 64 rows x 256 columns of one slice each --
+// in one global order g = slice * P + tile (P tiles per slice).  Each CTA
+// has two compute groups of eight warps and one control warp:
+//   * compute group k of CTA b (group index q = 2b + k of Gq = 2 * grid)
+//     quantises tiles q, q + Gq, q + 2Gq, ... from a two-stage ring.  It
+//     waits only on the stage's `full` barrier, which completes when the
+//     copy has landed and the control warp has placed the tile's slice
+//     encode factor E beside it, and releases the stage on its `empty`
+//     barrier.  It never waits on the rest of the grid.
+//   * the control warp issues every copy, and computes the slice amax in
+//     the same pass over the stack (S1): it streams this CTA's look-ahead
+//     tiles (the same tile indices as its two groups, up to L tiles ahead
+//     of them) through a two-stage ring, reduces each to its magnitude
+//     maximum, and keeps the per-slice results described below.
+// The look-ahead copies use the L2 evict-last policy and the quantising
+// copies (the same bytes, later) evict-first: the look-ahead read is the
+// HBM read, the second read hits L2, which holds the window of about L
+// tiles (32 KiB each); L = P + lead waves of Gq tiles.
+//
+// Per slice s, word ts[s] (the tensor_scale output, zeroed first) counts
+// the look-ahead tiles reduced so far, until it holds the slice's result.
+// The control warp folds each tile's maximum into amax[s] with an atomic
+// max at once and adds its CTA's tile count for a slice to ts[s] in one
+// release add when its look-ahead moves on to the next slice (by then its
+// earlier atomics have completed, so the release costs little).  The CTA
+// whose add completes the count acquires, reads the complete amax[s] and
+// replaces ts[s] by DONE | bits(G_s) (the sign bit marks it: a count never
+// has it, and G_s >= 0).  E for a tile comes from that word alone.
+//
+// Every wait ends.  The look-ahead stream waits only for its own ring and
+// for its window, la <= (the least tile its groups still need E for) + L.
+// A group waiting for slice s holds that least tile inside slice s, so the
+// window admits every look-ahead tile below (s + 1) P + lead Gq; with
+// lead >= 1 that includes the CTA's first look-ahead tile in slice s + 1,
+// whose arrival publishes the CTA's slice-s count.  By induction over the
+// slices every count is published, and all CTAs are resident (cooperative
+// launch).  The waits are bounded all the same.  With the amax given
+// (L = 0) there is no look-ahead.
+//
+// Per tile, from the staged input (four TMA boxes of 64 x 64 bf16, 128-byte
+// swizzle):
 //   rowwise pass   : 1024 blocks of 1x16, four per thread, results stored
 //                    straight to global (8 code bytes + 1 scale byte);
 //   columnwise pass: 256 units of 16 rows x 4 columns, one per thread, each
@@ -121,20 +110,29 @@ cudaError_t launch_amax(const uint16_t* w, int64_t nexp, int64_t per_slice, floa
 //                    results are staged and written as contiguous runs of the
 //                    transposed [in, out/2] layout.
 // Inside a swizzled box, 16-byte chunk c of row r sits at chunk c ^ (r & 7).
-// CTAs per SM: the dual kernel keeps two (128 registers; at three it spills
-// and runs 29 % slower), the rowwise-only kernel three (64 registers; 4 %
-// faster than two).
-constexpr int kQtMinbDual = 2, kQtMinbRow = 3;
-constexpr int kTR = 64, kTC = 256, kQT = 256;
+constexpr int kTR = 64, kTC = 256;
 constexpr int kBoxC = 64;                       // box columns (128 bytes)
 constexpr int kBoxBytes = kTR * kBoxC * 2;      // 8 KiB
 constexpr int kInStage = kTR * kTC * 2;         // 32 KiB (four boxes)
 constexpr int kColCodes = 4 * kTC * 8;          // [rb][col] 8 bytes
 constexpr int kColScales = 4 * kTC;             // [rb][col] 1 byte
 constexpr int kColBuf = kColCodes + kColScales; // one tile's staged columnwise results
-// Shared memory of the rowwise-only (DUAL false) and dual-layout kernels.
+constexpr int kQGroups = 2;                     // compute groups per CTA
+constexpr int kQGT = 256;                       // threads per compute group
+// Four compute warpgroups and one control warpgroup, of which one warp
+// works (96 registers per thread: the compute path fits them unspilled).
+constexpr int kQThreads = kQGroups * kQGT + 128;
 template <bool DUAL>
-constexpr int quant_smem() { return 2 * kInStage + (DUAL ? kColBuf : 0) + kScaleTableBytes + 64; }
+__host__ __device__ constexpr int group_bytes() { return 2 * kInStage + (DUAL ? kColBuf : 0); }
+// look-ahead stages: as many as fit beside the groups' buffers
+template <bool DUAL>
+__host__ __device__ constexpr int la_stages() { return DUAL ? 2 : 3; }
+// the groups' stages (and staging), the look-ahead stages, the E4M3 table,
+// the barriers, the E slots and a few words
+template <bool DUAL>
+constexpr int quant_smem() {
+  return kQGroups * group_bytes<DUAL>() + la_stages<DUAL>() * kInStage + kScaleTableBytes + 256;
+}
 constexpr uint32_t kWaitTries = 1u << 22;
 
 struct QuantTileArgs {  // aligned as CUtensorMap requires
@@ -143,132 +141,105 @@ struct QuantTileArgs {  // aligned as CUtensorMap requires
   uint8_t* scales_row;
   uint8_t* codes_col;
   uint8_t* scales_col;
-  const float* amax;      // complete for this launch's slices
-  float* tensor_scale;
+  float* amax;            // L > 0: accumulated here (zeroed first); L = 0: given
+  uint32_t* ts;           // L > 0: the per-slice words described above (zeroed first)
   int* status;
   int rows, cols;         // per slice
   int tiles_c;            // column tiles per slice
-  uint32_t ntiles;        // tiles of this launch
-  FastDiv per_exp;        // tiles per slice
+  int ntiles;             // tiles of the stack
+  int la;                 // look-ahead distance L in tiles (0: amax given)
+  FastDiv per_exp;        // tiles per slice (P)
   FastDiv by_tiles_c;
-  uint32_t e0;            // first slice of this launch
-  uint32_t nexp;          // slices in the whole stack
-  uint32_t ahead;         // > 0: also reduce the amax of slice e + ahead (0: off)
-  const uint16_t* w;      // the stack (for the look-ahead amax reads)
-  float* amax_out;        // the look-ahead amax accumulators (same array as amax)
   int tiled;              // block scales in the tensor-core tiled layout
   int ct_row, ct_col;     // tiled layout: tiles per tile row (rowwise, columnwise)
   int64_t sl_row, sl_col; // tiled layout: bytes per slice (rowwise, columnwise)
   int col32;              // codes_col is 32-byte aligned
 };
 
-template <bool F46, bool DUAL>
-__global__ void __launch_bounds__(kQT, DUAL ? kQtMinbDual : kQtMinbRow) k_quant_tiles(const __grid_constant__ QuantTileArgs A) {
-  // The kernel has no static shared memory, so the dynamic block starts at
-  // the (1 KiB aligned) base of the CTA's window, as the swizzled TMA boxes
-  // require; a misaligned base is reported instead of used.
-  extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* const in0 = smem;
-  unsigned char* const colc = smem + 2 * kInStage;  // DUAL: kColBuf bytes
-  unsigned char* const cols_s = colc + kColCodes;
-  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(colc + (DUAL ? kColBuf : 0));
-  uint64_t* const bar = reinterpret_cast<uint64_t*>(colc + (DUAL ? kColBuf : 0) + kScaleTableBytes);
-  float* const s_E = reinterpret_cast<float*>(bar + 2);
-  const int tid = threadIdx.x;
-  if (smem_u32(smem) & 1023u) {
-    if (tid == 0 && A.status) atomicOr(A.status, kStatusTimeout);
-    return;
-  }
-  const float six_m = F46 ? 1536.0f : 2688.0f;
-  const int rows = A.rows, cols = A.cols;
-  const int64_t cols_h = cols >> 1, cols_16 = cols >> 4, rows_h = rows >> 1, rows_16 = rows >> 4;
+struct QTile { uint32_t e; int r0, c0, rv, cv; };
 
-  build_scale_table(tbl);
-  if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
+__device__ __forceinline__ QTile qtile_of(const QuantTileArgs& A, int t) {
+  QTile T;
+  const uint32_t e = A.per_exp.div((uint32_t)t);
+  const uint32_t rem = (uint32_t)t - e * A.per_exp.d;
+  const uint32_t tr = A.by_tiles_c.div(rem);
+  const uint32_t tc = rem - tr * (uint32_t)A.tiles_c;
+  T.e = e;
+  T.r0 = (int)tr * kTR;
+  T.c0 = (int)tc * kTC;
+  T.rv = min(kTR, A.rows - T.r0);
+  T.cv = min(kTC, A.cols - T.c0);
+  return T;
+}
 
-  struct Tile { uint32_t e; int r0, c0, rv, cv; bool first; };
-  auto tile_of = [&](uint32_t t) {
-    Tile T;
-    const uint32_t el = A.per_exp.div(t);
-    const uint32_t rem = t - el * A.per_exp.d;
-    T.e = A.e0 + el;
-    const uint32_t tr = A.by_tiles_c.div(rem);
-    const uint32_t tc = rem - tr * (uint32_t)A.tiles_c;
-    T.r0 = (int)tr * kTR;
-    T.c0 = (int)tc * kTC;
-    T.rv = min(kTR, rows - T.r0);
-    T.cv = min(kTC, cols - T.c0);
-    T.first = rem == 0;
-    return T;
-  };
-
-  // producer: thread 0 arms the stage barrier with the tile's byte count and
-  // issues the four box loads (out-of-range parts are zero-filled), then
-  // forms the slice's encode factor for the consumers.
-  auto issue = [&](uint32_t t, int st) {
-    if (tid == 0 && t < A.ntiles) {
-      const Tile T = tile_of(t);
-      mbar_arrive_expect_tx(&bar[st], kInStage);
-      const int y = (int)(T.e * (uint32_t)rows) + T.r0;
+// Thread `lane 0` of the control warp: the four box loads of tile t into
+// `dst`, completing on `b` (parts out of range are zero-filled).
+__device__ __forceinline__ void qload_tile(const QuantTileArgs& A, int t, unsigned char* dst,
+                                           uint64_t* b, uint64_t pol) {
+  const QTile T = qtile_of(A, t);
+  mbar_arrive_expect_tx(b, kInStage);
+  const int y = (int)(T.e * (uint32_t)A.rows) + T.r0;
 #pragma unroll
-      for (int j = 0; j < kTC / kBoxC; j++)
-        tma_load_2d(in0 + st * kInStage + j * kBoxBytes, &A.tmap, T.c0 + j * kBoxC, y, &bar[st]);
-      const float am = A.amax[T.e];
-      float G, E;
-      global_scales(am, six_m, G, E);
-      s_E[st] = E;
-      if (T.first) {
-        A.tensor_scale[T.e] = G;
-        if (A.status && !isfinite(am)) atomicOr(A.status, kStatusNonFinite);
-      }
-    }
-  };
+  for (int j = 0; j < kTC / kBoxC; j++)
+    tma_load_2d_hint(dst + j * kBoxBytes, &A.tmap, T.c0 + j * kBoxC, y, b, pol);
+}
 
-  const uint32_t t0 = blockIdx.x;
-  issue(t0, 0);
-  issue(t0 + gridDim.x, 1);
-
-  // rowwise geometry of this thread: 16-column block cb, rows (tid >> 4) + 16k
-  const int cb = tid & 15, rb0 = tid >> 4;
+// ---- compute group k (threads tg = 0 .. 255 of the group)
+template <bool F46, bool DUAL>
+__device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned char* gbase,
+                                            const ScaleEnt* tbl, uint64_t* full, uint64_t* empty,
+                                            const float* s_E, int k, int tg) {
+  const int rows = A.rows, cols = A.cols, N = A.ntiles;
+  const int Gq = kQGroups * gridDim.x;
+  const int64_t cols_h = cols >> 1, cols_16 = cols >> 4, rows_h = rows >> 1, rows_16 = rows >> 4;
+  unsigned char* const colc = gbase + 2 * kInStage;  // DUAL: kColBuf bytes
+  unsigned char* const cols_s = colc + kColCodes;
+  const int warp = tg >> 5, lane = tg & 31;
+  // rowwise geometry: 16-column block cb of rows rb0 + 16k.  In each
+  // quarter warp the lanes of odd boxes take the other row of the row pair,
+  // so their 16-byte loads fall in the other half of the banks.
+  const int cb = tg & 15;
+  const int rb0 = 2 * warp + (((tg >> 4) ^ (tg >> 2)) & 1);
   const int rbox = (cb >> 2) * kBoxBytes, rchunk = 2 * (cb & 3);
   // columnwise geometry: row block cr, columns 4q .. 4q+3
-  const int warp = tid >> 5, lane = tid & 31;
   const int cr = warp >> 1, q = ((warp & 1) << 5) + lane;
   const int cbox = (q >> 4) * kBoxBytes, cchunk = (q & 15) >> 1, chalf = (q & 1) * 8;
+  // columnwise staging: columns 4q..4q+1 and 4q+2..4q+3 fill the two
+  // 16-byte halves of a 32-byte group, in swapped order for odd q >> 2, so
+  // a quarter warp's 16-byte stores cover all banks.
+  const int hsw = (q >> 2) & 1;
 
   // The columnwise results of a tile, staged in shared memory (codes
-  // [rb][col] 8 bytes, then scales [rb][col] 1 byte), leave as contiguous
-  // runs of the transposed layout: thread c writes column c.
-  auto write_col = [&](const Tile& T) {
-    const int c = tid;
+  // [rb][col] 8 bytes, the two halves of each 32-byte group swapped as
+  // above, then scales [rb][col] 1 byte), leave as contiguous runs of the
+  // transposed layout: thread c writes column c.
+  auto write_col = [&](const QTile& T) {
+    const int c = tg;
     if (c < T.cv) {
       const int nrb = T.rv >> 4;
       const int64_t grow = (int64_t)T.e * cols + T.c0 + c;
       uint8_t* dstc = A.codes_col + grow * rows_h + (T.r0 >> 1);
       uint8_t* dsts = A.scales_col + grow * rows_16 + (T.r0 >> 4);
+      const int soff = (c >> 2) * 32 + ((((c >> 1) & 1) ^ ((c >> 4) & 1)) << 4) + (c & 1) * 8;
       if (nrb == 4 && (rows & 31) == 0) {
-        const uint2 v0 = *reinterpret_cast<const uint2*>(colc + c * 8);
-        const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + c * 8);
-        const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + c * 8);
-        const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + c * 8);
+        const uint2 v0 = *reinterpret_cast<const uint2*>(colc + soff);
+        const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + soff);
+        const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + soff);
+        const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + soff);
         if (A.col32 && (rows & 63) == 0) {
           // the run is 32-byte aligned: one full-sector store (half the
           // write requests of two 16-byte stores)
           const uint32_t v8[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
-          stg256(dstc, v8);
+          stg256_stream(dstc, v8);
         } else {
-          reinterpret_cast<uint4*>(dstc)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
-          reinterpret_cast<uint4*>(dstc)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+          stg_stream(dstc, make_uint4(v0.x, v0.y, v1.x, v1.y));
+          stg_stream(dstc + 16, make_uint4(v2.x, v2.y, v3.x, v3.y));
         }
       } else {
-        for (int rb = 0; rb < nrb; rb++)
-          *reinterpret_cast<uint2*>(dstc + rb * 8) =
-              *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + c * 8);
+        for (int rb = 0; rb < nrb; rb++) {
+          const uint2 v = *reinterpret_cast<const uint2*>(colc + rb * (kTC * 8) + soff);
+          stg_stream_v2(dstc + rb * 8, v.x, v.y);
+        }
       }
       if (A.tiled) {
         // the tile's four row blocks are block columns r0/16 .. +3, a
@@ -286,52 +257,27 @@ __global__ void __launch_bounds__(kQT, DUAL ? kQtMinbDual : kQtMinbRow) k_quant_
         const uint32_t sc = (uint32_t)cols_s[c] | ((uint32_t)cols_s[kTC + c] << 8) |
                             ((uint32_t)cols_s[2 * kTC + c] << 16) |
                             ((uint32_t)cols_s[3 * kTC + c] << 24);
-        *reinterpret_cast<uint32_t*>(dsts) = sc;
+        stg_stream_u32(dsts, sc);
       } else {
-        for (int rb = 0; rb < nrb; rb++) dsts[rb] = cols_s[rb * kTC + c];
+        for (int rb = 0; rb < nrb; rb++) stg_stream_u8(dsts + rb, cols_s[rb * kTC + c]);
       }
     }
   };
 
-  // The rowwise-only kernel has one barrier per tile: the barrier that
-  // opens tile t + 1 also frees tile t's input stage, which then takes the
-  // copy two tiles ahead.  The dual kernel needs a second barrier between
-  // the columnwise pass and the write-out of its staged results, and frees
-  // the stage there.
-  int st = 0;
-  uint32_t it = 0;
-  for (uint32_t t = t0; t < A.ntiles; t += gridDim.x, st ^= 1, it++) {
-    const bool ok = mbar_wait(&bar[st], (it >> 1) & 1, kWaitTries);
-    if (__syncthreads_or(!ok)) {  // a copy never landed: report and stop
-      if (tid == 0 && A.status) atomicOr(A.status, kStatusTimeout);
-      // the other stage's copy, if one is in flight
-      if (DUAL || it == 0) mbar_wait(&bar[st ^ 1], ((it + 1) >> 1) & 1, kWaitTries);
+  const int bar_id = 1 + k;
+  int j = 0;
+  for (int g = kQGroups * (int)blockIdx.x + k; g < N; g += Gq, j++) {
+    const int st = j & 1;
+    const bool ok = mbar_wait(&full[2 * k + st], (j >> 1) & 1, kWaitTries);
+    // The whole group agrees to go on, and the previous tile's staged
+    // results have been written out by every thread.
+    if (named_barrier_or(bar_id, kQGT, !ok)) {
+      if (tg == 0 && A.status) atomicOr(A.status, kStatusTimeout);
       return;
     }
-    if (!DUAL && it > 0) issue(t + gridDim.x, st ^ 1);
-    const Tile T = tile_of(t);
-    const float E = s_E[st];
-    const unsigned char* tile = in0 + st * kInStage;
-
-    // look-ahead amax: the same tile position of slice e + ahead is read now
-    // and reduced after the rowwise pass, whose arithmetic covers the load
-    // latency (the dual kernel is bound by instruction issue, so these reads
-    // use HBM bandwidth it leaves idle).
-    const bool ahead = DUAL && A.ahead != 0 && T.e + A.ahead < A.nexp;
-    uint32_t sh[4][8];
-    if (ahead) {
-      const uint16_t* base = A.w + ((int64_t)(T.e + A.ahead) * rows + T.r0) * cols + T.c0;
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const int id = tid + i * kQT, r = id >> 4, c = (id & 15) * 16;
-        if (r < T.rv && c < T.cv) {
-          ldg32(base + (int64_t)r * cols + c, sh[i]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; k++) sh[i][k] = 0;
-        }
-      }
-    }
+    const float E = s_E[2 * k + st];
+    const unsigned char* tile = gbase + st * kInStage;
+    const QTile T = qtile_of(A, g);
 
     // rowwise blocks: four per thread, 16 rows apart
     {
@@ -340,8 +286,8 @@ __global__ void __launch_bounds__(kQT, DUAL ? kQtMinbDual : kQtMinbRow) k_quant_
       uint8_t* ps = A.scales_row + grow0 * cols_16 + (T.c0 >> 4) + cb;
       const bool cvalid = cb * 16 < T.cv;
 #pragma unroll 1
-      for (int k = 0; k < 4; k++) {
-        const int r = rb0 + 16 * k;
+      for (int kk = 0; kk < 4; kk++) {
+        const int r = rb0 + 16 * kk;
         if (cvalid && r < T.rv) {
           const unsigned char* rowp = tile + rbox + r * 128;
           const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((rchunk ^ (r & 7)) << 4));
@@ -349,26 +295,14 @@ __global__ void __launch_bounds__(kQT, DUAL ? kQtMinbDual : kQtMinbRow) k_quant_
           const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
           uint32_t c0w, c1w, sb;
           quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
-          *reinterpret_cast<uint2*>(pc + 16 * k * cols_h) = make_uint2(c0w, c1w);
+          stg_stream_v2(pc + 16 * kk * cols_h, c0w, c1w);
           if (A.tiled)
             A.scales_row[T.e * A.sl_row +
                          scale_off_tiled(T.r0 + r, (T.c0 >> 4) + cb, A.ct_row)] = (uint8_t)sb;
           else
-            ps[16 * k * cols_16] = (uint8_t)sb;
+            stg_stream_u8(ps + 16 * kk * cols_16, sb);
         }
       }
-    }
-
-    if (ahead) {
-      uint32_t m = maxabs2_nan(sh[0][0], sh[0][1]);
-#pragma unroll
-      for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int k = 0; k < 8; k++)
-          if (i > 0 || k > 1) m = maxabs2_nan(m, sh[i][k]);
-      uint32_t mm = maxabs2_nan(m, __byte_perm(m, 0, 0x1032)) & 0x7fff0000u;  // FP32 bits
-      mm = __reduce_max_sync(0xffffffffu, mm);
-      if ((tid & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(A.amax_out + T.e + A.ahead), mm);
     }
 
     if (DUAL) {
@@ -382,21 +316,302 @@ __global__ void __launch_bounds__(kQT, DUAL ? kQtMinbDual : kQtMinbRow) k_quant_
           wa[i] = v.x;
           wb[i] = v.y;
         }
+        unsigned char* const cq = colc + cr * (kTC * 8) + q * 32;
         uint32_t cj[2], ck[2], sbj, sbk, sw;
         quant_col_pair<F46>(wa, E, tbl, cj, ck, sbj, sbk);
-        *reinterpret_cast<uint4*>(colc + cr * (kTC * 8) + q * 32) =
-            make_uint4(cj[0], cj[1], ck[0], ck[1]);
+        *reinterpret_cast<uint4*>(cq + hsw * 16) = make_uint4(cj[0], cj[1], ck[0], ck[1]);
         sw = sbj | (sbk << 8);
         quant_col_pair<F46>(wb, E, tbl, cj, ck, sbj, sbk);
-        *reinterpret_cast<uint4*>(colc + cr * (kTC * 8) + q * 32 + 16) =
-            make_uint4(cj[0], cj[1], ck[0], ck[1]);
+        *reinterpret_cast<uint4*>(cq + (hsw ^ 1) * 16) = make_uint4(cj[0], cj[1], ck[0], ck[1]);
         sw |= (sbj << 16) | (sbk << 24);
         *reinterpret_cast<uint32_t*>(cols_s + cr * kTC + q * 4) = sw;
       }
-      __syncthreads();
-      issue(t + 2 * gridDim.x, st);
-      write_col(T);
     }
+    named_barrier(bar_id, kQGT);  // the stage is read; the staged results are complete
+    if (tg == 0) mbar_arrive(&empty[2 * k + st]);
+    if (DUAL) write_col(T);
+  }
+}
+
+// ---- the control warp: copies of the tiles to quantise, and E beside them
+template <bool F46>
+__device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned char* smem,
+                                              int gbytes, uint64_t* full, uint64_t* empty,
+                                              float* s_E, volatile int* s_least) {
+  const float six_m = F46 ? 1536.0f : 2688.0f;
+  const int lane = threadIdx.x & 31, N = A.ntiles, L = A.la;
+  const int Gq = kQGroups * gridDim.x;
+  const int q0 = kQGroups * (int)blockIdx.x;  // this CTA's first group index
+  uint64_t pol = 0;
+  if (lane == 0) pol = l2_policy_evict_first();
+  // per group: next iteration to load, next iteration to give E
+  int qi[kQGroups], qe[kQGroups];
+#pragma unroll
+  for (int k = 0; k < kQGroups; k++) qi[k] = qe[k] = 0;
+  // E of the last finished slice; per group, the slice whose word lane 0
+  // is reading and that word
+  int e_s = -1;
+  float e_E = 0.0f;
+  int pf_s[kQGroups];
+  uint32_t pf_w[kQGroups];
+#pragma unroll
+  for (int k = 0; k < kQGroups; k++) {
+    pf_s[k] = -1;
+    pf_w[k] = 0;
+  }
+  uint64_t t_idle = globaltimer_ns();
+  bool failed = false;
+  while (true) {
+    bool prog = false;
+    // (1) copies of tiles to quantise, into stages their group has released
+#pragma unroll
+    for (int k = 0; k < kQGroups; k++) {
+      const int g = q0 + k + qi[k] * Gq;
+      if (g < N) {
+        int freed = 1;
+        if (qi[k] >= 2 && lane == 0)
+          freed = mbar_test(&empty[2 * k + (qi[k] & 1)], ((qi[k] - 2) >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, freed, 0)) {
+          if (lane == 0)
+            qload_tile(A, g, smem + k * gbytes + (qi[k] & 1) * kInStage,
+                       &full[2 * k + (qi[k] & 1)], pol);
+          qi[k]++;
+          prog = true;
+        }
+      }
+    }
+    // (2) E beside each loaded tile, once its slice is finished
+#pragma unroll
+    for (int k = 0; k < kQGroups; k++) {
+      if (qe[k] < qi[k]) {
+        const int g = q0 + k + qe[k] * Gq;
+        const int s = (int)A.per_exp.div((uint32_t)g);
+        int have = 0;
+        float E = 0.0f;
+        if (L == 0) {
+          float Gs;
+          global_scales(A.amax[s], six_m, Gs, E);
+          have = 1;
+        } else if (s == e_s) {
+          E = e_E;
+          have = 1;
+        } else {
+          if (lane == 0) {
+            if (pf_s[k] == s && (pf_w[k] & kSliceDone)) {
+              have = 1;
+            } else {
+              pf_w[k] = ld_relaxed_u32(A.ts + s);  // looked at in the next round
+              pf_s[k] = s;
+            }
+          }
+          have = __shfl_sync(0xffffffffu, have, 0);
+          if (have) {
+            const uint32_t w = __shfl_sync(0xffffffffu, pf_w[k], 0);
+            const float Gs = __uint_as_float(w & ~kSliceDone);
+            E = fminf(__frcp_rn(Gs), FLT_MAX);
+            e_s = s;
+            e_E = E;
+          }
+        }
+        if (have) {
+          if (lane == 0) {
+            s_E[2 * k + (qe[k] & 1)] = E;
+            mbar_arrive(&full[2 * k + (qe[k] & 1)]);
+          }
+          qe[k]++;
+          prog = true;
+        }
+      }
+    }
+    // the least tile the groups still need E for bounds the look-ahead
+    int least = N;
+#pragma unroll
+    for (int k = 0; k < kQGroups; k++) least = min(least, q0 + k + qe[k] * Gq);
+    if (lane == 0 && prog) *s_least = least;
+    if (least >= N) break;
+    // lane 0 decides when nothing has moved for too long
+    int stalled = 0;
+    if (lane == 0) {
+      const uint64_t now = globaltimer_ns();
+      if (prog) t_idle = now;
+      else stalled = now - t_idle > kMaxWaitNs;
+    }
+    if (__shfl_sync(0xffffffffu, stalled, 0)) {
+      failed = true;
+      break;
+    }
+  }
+  if (failed && lane == 0) {
+    // Nothing moved for too long (a copy never landed or a slice never
+    // finished): report, and give the groups what they wait for so that
+    // they stop on their own.
+    if (A.status) atomicOr(A.status, kStatusTimeout);
+    for (int k = 0; k < kQGroups; k++)
+      for (; qe[k] < qi[k]; qe[k]++) {
+        s_E[2 * k + (qe[k] & 1)] = 0.0f;
+        mbar_arrive(&full[2 * k + (qe[k] & 1)]);
+      }
+  }
+}
+
+// ---- the look-ahead stream (kLaThreads threads, two warps): this CTA's
+// look-ahead tiles in increasing order, n -> q0 + n % 2 + (n / 2) Gq, each
+// copied into a ring of S stages, reduced to its magnitude maximum (bf16 bit
+// patterns, exact; NaN propagates) and counted into the per-slice words.
+// Rows past the slice (a ragged last row tile) belong to the next slice and
+// are left out; columns past the slice are zero-filled by the copy.
+constexpr int kLaThreads = 64;
+template <bool F46, int S>
+__device__ __forceinline__ void quant_lookahead(const QuantTileArgs& A, unsigned char* lab,
+                                                uint64_t* lafull, uint32_t* s_lamax,
+                                                const volatile int* s_least) {
+  const float six_m = F46 ? 1536.0f : 2688.0f;
+  const int lt = threadIdx.x - (kQGroups * kQGT + 32), lane = lt & 31, lw = lt >> 5;
+  const int N = A.ntiles, L = A.la;
+  const int Gq = kQGroups * gridDim.x;
+  const int q0 = kQGroups * (int)blockIdx.x;
+  const uint32_t P = A.per_exp.d;
+  int la_count = 0;
+  for (int k = 0; k < kQGroups; k++)
+    if (q0 + k < N) la_count += (N - 1 - (q0 + k)) / Gq + 1;
+  auto la_tile = [&](int n) { return q0 + (n % kQGroups) + (n / kQGroups) * Gq; };
+  uint64_t pol = 0;
+  if (lt == 0) pol = l2_policy_evict_last();
+  // thread 0 of the stream: this CTA's unpublished count, and the last add
+  int pend_s = -1, chk_s = -1;
+  uint32_t pend_n = 0, chk_old = 0, chk_n = 0;
+  auto finish_if_last = [&]() {
+    if (chk_s >= 0 && chk_old + chk_n == P) {
+      fence_acq_rel_gpu();
+      float Gs, Es;
+      global_scales(ld_relaxed_f32(A.amax + chk_s), six_m, Gs, Es);
+      st_relaxed_u32(A.ts + chk_s, kSliceDone | __float_as_uint(Gs));
+    }
+    chk_s = -1;
+  };
+  auto publish = [&]() {
+    finish_if_last();
+    if (pend_s >= 0) {
+      chk_old = atom_add_release(A.ts + pend_s, pend_n);
+      chk_s = pend_s;
+      chk_n = pend_n;
+    }
+    pend_s = -1;
+    pend_n = 0;
+  };
+  // thread 0: copy look-ahead tile n once the window admits it (bounded)
+  auto issue = [&](int n) -> bool {
+    const int t = la_tile(n);
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; t > *s_least + L; i++) {
+      finish_if_last();  // nothing of ours may be held while we wait
+      const uint64_t now = globaltimer_ns();
+      if (i == 0) t0 = now;
+      else if (now - t0 > kMaxWaitNs) return false;
+      __nanosleep(256);
+    }
+    qload_tile(A, t, lab + (n % S) * kInStage, &lafull[n % S], pol);
+    return true;
+  };
+  int issued = 0;
+  bool ok = true;
+  if (lt == 0)
+    for (; issued < S && issued < la_count && ok; issued++) ok = issue(issued);
+  for (int n = 0; n < la_count; n++) {
+    const int st = n % S;
+    bool landed = __shfl_sync(0xffffffffu, (int)ok, 0) && mbar_wait(&lafull[st], (n / S) & 1, kWaitTries);
+    uint32_t m[4] = {0, 0, 0, 0};
+    if (landed) {
+      const int rv = min(kTR, A.rows - (int)A.by_tiles_c.div((uint32_t)la_tile(n) -
+                                                             A.per_exp.div((uint32_t)la_tile(n)) * P) *
+                                           kTR);
+      // thread lt reads 16-byte chunks lt + 64 i: row (lt >> 3) + 8 (i & 7) of its box
+      const unsigned char* p = lab + st * kInStage + lt * 16;
+#pragma unroll 8
+      for (int i = 0; i < kInStage / (16 * kLaThreads); i++) {
+        if ((lt >> 3) + 8 * (i & 7) < rv) {
+          const uint4 v = *reinterpret_cast<const uint4*>(p + i * 16 * kLaThreads);
+          m[i & 3] = maxabs2_nan(m[i & 3], maxabs2_nan(maxabs2_nan(v.x, v.y), maxabs2_nan(v.z, v.w)));
+        }
+      }
+    }
+    uint32_t mm = maxabs2_nan(maxabs2_nan(m[0], m[1]), maxabs2_nan(m[2], m[3]));
+    mm = maxabs2_nan(mm, __byte_perm(mm, 0, 0x1032)) & 0x7fff0000u;  // FP32 bits
+    mm = __reduce_max_sync(0xffffffffu, mm);
+    if (lane == 0) s_lamax[2 * (n & 1) + lw] = mm;
+    if (named_barrier_or(3, kLaThreads, !landed)) {
+      // a look-ahead copy never landed: report and stop, after the copies
+      // still in flight
+      if (lt == 0) {
+        if (A.status) atomicOr(A.status, kStatusTimeout);
+        for (int i = n + 1; i < issued; i++) mbar_wait(&lafull[i % S], (i / S) & 1, kWaitTries);
+      }
+      return;
+    }
+    if (lt == 0) {
+      const uint32_t mx = max(s_lamax[2 * (n & 1)], s_lamax[2 * (n & 1) + 1]);
+      finish_if_last();  // the add published earlier has returned by now
+      const int s = (int)A.per_exp.div((uint32_t)la_tile(n));
+      if (s != pend_s) publish();  // before this tile's atomic: nothing left in flight
+      atomicMax(reinterpret_cast<unsigned int*>(A.amax + s), mx);
+      pend_s = s;
+      pend_n++;
+      if (n + 1 == la_count) {  // this CTA's last look-ahead tile
+        publish();
+        finish_if_last();
+      }
+      if (ok && issued < la_count) {  // the stage just read takes tile n + S
+        ok = issue(issued);
+        issued++;
+        if (!ok && A.status) atomicOr(A.status, kStatusTimeout);
+      }
+    }
+  }
+}
+
+template <bool F46, bool DUAL>
+__global__ void __launch_bounds__(kQThreads, 1) k_quant_tiles(const __grid_constant__ QuantTileArgs A) {
+  // The kernel has no static shared memory, so the dynamic block starts at
+  // the (1 KiB aligned) base of the CTA's window, as the swizzled TMA boxes
+  // require; a misaligned base is reported instead of used.
+  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int kG = group_bytes<DUAL>();
+  constexpr int kS = la_stages<DUAL>();
+  unsigned char* const lab = smem + kQGroups * kG;
+  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(lab + kS * kInStage);
+  uint64_t* const full = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(tbl) +
+                                                     kScaleTableBytes);  // [group][stage]
+  uint64_t* const empty = full + 2 * kQGroups;                           // [group][stage]
+  uint64_t* const lafull = empty + 2 * kQGroups;                         // [look-ahead stage]
+  float* const s_E = reinterpret_cast<float*>(lafull + kS);              // [group][stage]
+  uint32_t* const s_lamax = reinterpret_cast<uint32_t*>(s_E + 2 * kQGroups);  // [2][warp]
+  int* const s_least = reinterpret_cast<int*>(s_lamax + 4);
+  const int tid = threadIdx.x;
+  const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+  if (!misaligned) {
+    build_scale_table(tbl);
+    if (tid == 0) {
+      for (int i = 0; i < 2 * kQGroups; i++) {
+        mbar_init(&full[i], 2);   // the copy's arrival with its bytes, and E's
+        mbar_init(&empty[i], 1);  // the group's release
+      }
+      for (int i = 0; i < kS; i++) mbar_init(&lafull[i], 1);
+      *s_least = kQGroups * (int)blockIdx.x;
+      fence_barrier_init();
+    }
+  } else if (tid == 0 && A.status) {
+    atomicOr(A.status, kStatusTimeout);
+  }
+  __syncthreads();
+  constexpr int kCtl = kQGroups * kQGT;  // the control warp, then the look-ahead warps
+  if (misaligned || tid >= kCtl + 32 + kLaThreads) return;
+  if (tid >= kCtl + 32) {
+    if (A.la > 0) quant_lookahead<F46, kS>(A, lab, lafull, s_lamax, s_least);
+  } else if (tid >= kCtl) {
+    quant_control<F46>(A, smem, kG, full, empty, s_E, s_least);
+  } else {
+    quant_group<F46, DUAL>(A, smem + (tid / kQGT) * kG, tbl, full, empty, s_E, tid / kQGT,
+                           tid % kQGT);
   }
 }
 
@@ -409,16 +624,67 @@ static cudaError_t set_quant_smem() {
   });
 }
 
+// CTAs of k_quant_tiles<F46, DUAL> resident per SM (the cooperative grid's
+// limit), once per device.
+template <bool F46, bool DUAL>
+static int quant_occupancy(cudaError_t* err) {
+  static PerDeviceInt occ;
+  return occ.get(
+      [](cudaError_t* e) {
+        int b = 0;
+        *e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_quant_tiles<F46, DUAL>, kQThreads,
+                                                           quant_smem<DUAL>());
+        return b;
+      },
+      err);
+}
+
+template <bool F46, bool DUAL>
+static cudaError_t launch_quant_kernel(const QuantTileArgs& A, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = quant_smem<DUAL>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_quant_tiles<F46, DUAL>, A);
+}
+
+template <bool F46, bool DUAL>
+static cudaError_t run_quant(QuantTileArgs& A, int64_t per, cudaStream_t s) {
+  const DevInfo* di = device_info();
+  cudaError_t err = set_quant_smem<F46, DUAL>();
+  if (err != cudaSuccess) return err;
+  const int occ = quant_occupancy<F46, DUAL>(&err);
+  if (err != cudaSuccess) return err;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  // one CTA per compute-group pair of tiles; no more CTAs than resident
+  const int grid = (int)std::min<int64_t>(((int64_t)A.ntiles + kQGroups - 1) / kQGroups,
+                                          (int64_t)occ * di->sms);
+  // Look-ahead distance: one slice of tiles plus a lead of a few waves of
+  // the grid's compute groups (see above); 0 when the amax is given.
+  if (A.la) {
+    const int64_t la =
+        per + (int64_t)g_quant_lead_waves.load(std::memory_order_relaxed) * kQGroups * grid;
+    if (la + A.ntiles >= (1ll << 31)) return cudaErrorInvalidValue;
+    A.la = (int)la;
+  }
+  return launch_quant_kernel<F46, DUAL>(A, grid, s);
+}
+
 cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int cols, bool f46,
                                uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
                                uint8_t* scales_col, float* amax, float* tensor_scale,
                                int* status, bool compute_amax, bool tiled, cudaStream_t s) {
-  const DevInfo* di = device_info();
   const int tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
   const int64_t per = (int64_t)tiles_r * tiles_c;
   const int64_t ntiles = nexp * per;
   if (ntiles == 0) return cudaSuccess;
-  if (ntiles >= (1ll << 31) - (1ll << 24) || nexp * (int64_t)rows >= (1ll << 31))
+  if (ntiles >= (1ll << 30) || nexp * (int64_t)rows >= (1ll << 31))
     return cudaErrorInvalidValue;
   QuantTileArgs A;
   if (!encode_tmap_2d(&A.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, (uint64_t)cols,
@@ -430,77 +696,37 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
   A.codes_col = codes_col;
   A.scales_col = scales_col;
   A.amax = amax;
-  A.amax_out = amax;
-  A.tensor_scale = tensor_scale;
+  // The per-slice words live in tensor_scale until the final pass below
+  // overwrites them with the tensor scales.
+  A.ts = reinterpret_cast<uint32_t*>(tensor_scale);
   A.status = status;
   A.rows = rows;
   A.cols = cols;
   A.tiles_c = tiles_c;
+  A.ntiles = (int)ntiles;
+  A.la = compute_amax ? 1 : 0;
   A.per_exp.d = (uint32_t)per;
   make_fastdiv((uint32_t)per, &A.per_exp.m, &A.per_exp.s);
   A.by_tiles_c.d = (uint32_t)tiles_c;
   make_fastdiv((uint32_t)tiles_c, &A.by_tiles_c.m, &A.by_tiles_c.s);
-  A.nexp = (uint32_t)nexp;
-  A.w = w;
   A.tiled = tiled ? 1 : 0;
   A.ct_row = (cols / 16 + 3) / 4;
   A.ct_col = (rows / 16 + 3) / 4;
   A.sl_row = tiled_scale_bytes(rows, cols);
   A.sl_col = tiled_scale_bytes(cols, rows);
   A.col32 = (reinterpret_cast<uintptr_t>(codes_col) & 31) == 0;
-  const bool dual = codes_col != nullptr;
-  const int full_grid = di->sms * (dual ? kQtMinbDual : kQtMinbRow);
-  // Slices per launch: with the look-ahead amax every launch quantises one
-  // chunk while reducing the amax of the next, so each launch must see its
-  // chunk's amax complete.  Two costs set the chunk: every launch boundary
-  // (a partial last wave and the refill of the copy pipeline, about 16 us
-  // measured), and the separate amax pass over the first chunk (2 bytes per
-  // element at about 7 TB/s).  Their sum is smallest at
-  // chunk = sqrt(nexp * 16 us / amax time of one slice)
-  //       = sqrt(nexp * 5.6e7 / elements per slice),
-  // and a chunk is kept at 40 waves of tiles or more.
-  // The look-ahead is used by the dual-layout kernel only (the rowwise kernel
-  // is close to memory bound, where a separate reduction pass is as fast);
-  // its reads are 32-byte vectors, so it also needs a 32-byte aligned stack.
-  // Otherwise the whole amax is reduced by one pass up front.
-  const bool lookahead = compute_amax && codes_col != nullptr &&
-                         (reinterpret_cast<uintptr_t>(w) & 31) == 0;
-  int64_t chunk = nexp;
-  if (lookahead) {
-    const double balanced = std::floor(std::sqrt((double)nexp * 5.6e7 / ((double)rows * cols)) + 0.5);
-    chunk = std::max<int64_t>((int64_t)balanced, (40ll * full_grid + per - 1) / per);
-    chunk = std::max<int64_t>(chunk, 1);
-    // NVQ_QUANT_CHUNK (slices per launch) overrides the choice; the tests use
-    // it to exercise the look-ahead on small stacks.
-    if (const char* env = std::getenv("NVQ_QUANT_CHUNK")) {
-      const long long v = std::atoll(env);
-      if (v > 0) chunk = v;
-    }
-    chunk = std::min<int64_t>(chunk, nexp);
-  }
-  if (compute_amax) {
-    cudaError_t err = launch_amax(w, chunk, (int64_t)rows * cols, amax, s);
-    if (err != cudaSuccess) return err;
-  }
   cudaError_t err;
-  if (f46 && dual) err = set_quant_smem<true, true>();
-  else if (f46) err = set_quant_smem<true, false>();
-  else if (dual) err = set_quant_smem<false, true>();
-  else err = set_quant_smem<false, false>();
-  if (err != cudaSuccess) return err;
-  for (int64_t e0 = 0; e0 < nexp; e0 += chunk) {
-    const int64_t n = std::min<int64_t>(chunk, nexp - e0);
-    A.e0 = (uint32_t)e0;
-    A.ntiles = (uint32_t)(n * per);
-    A.ahead = (lookahead && e0 + chunk < nexp) ? (uint32_t)chunk : 0u;
-    const int grid = (int)std::min<int64_t>(n * per, full_grid);
-    if (f46 && dual) k_quant_tiles<true, true><<<grid, kQT, quant_smem<true>(), s>>>(A);
-    else if (f46) k_quant_tiles<true, false><<<grid, kQT, quant_smem<false>(), s>>>(A);
-    else if (dual) k_quant_tiles<false, true><<<grid, kQT, quant_smem<true>(), s>>>(A);
-    else k_quant_tiles<false, false><<<grid, kQT, quant_smem<false>(), s>>>(A);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (compute_amax) {
+    // amax accumulators and arrival counters start at zero
+    if ((err = launch_zero_f32(amax, nexp, s, tensor_scale)) != cudaSuccess) return err;
   }
-  return cudaSuccess;
+  const bool dual = codes_col != nullptr;
+  if (f46 && dual) err = run_quant<true, true>(A, per, s);
+  else if (f46) err = run_quant<true, false>(A, per, s);
+  else if (dual) err = run_quant<false, true>(A, per, s);
+  else err = run_quant<false, false>(A, per, s);
+  if (err != cudaSuccess) return err;
+  return launch_tensor_scales(amax, tensor_scale, nexp, f46, status, s);
 }
 
 // ------------------------------------------------------ per-token activations

@@ -162,6 +162,13 @@ def test_validation_before_any_device_work(nvq):
     assert L.nvq_debug_wait_timeout(1 << 20, ok16, P) == 3
     assert L.nvq_debug_wait_timeout(16, P, P) == 1
     assert L.nvq_debug_wait_timeout(16, _vp(FAKE + 2), P) == 2
+    assert L.nvq_debug_count_timeout(0, ok16, ok16, P) == 3
+    assert L.nvq_debug_count_timeout(1 << 20, ok16, ok16, P) == 3
+    assert L.nvq_debug_count_timeout(16, P, ok16, P) == 1
+    assert L.nvq_debug_count_timeout(16, ok16, P, P) == 1
+    assert L.nvq_debug_count_timeout(16, _vp(FAKE + 2), ok16, P) == 2
+    assert L.nvq_debug_set_quant_lead(1) == 3 and L.nvq_debug_set_quant_lead(9) == 3
+    assert L.nvq_debug_set_quant_lead(2) == 0
     # nested NF4 absmax
     assert L.nf4_absmax_nest(ok16, 1, (1 << 25) + 1, ok16, ok16, ok16, P, P) == 3
     assert L.nf4_absmax_nest(ok16, -1, 8, ok16, ok16, ok16, P, P) == 3

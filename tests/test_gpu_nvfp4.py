@@ -216,31 +216,59 @@ def test_stream_ordering_on_side_stream(nvq, oracle_mod):
     assert_same(u16(dt), oracle_mod.nvfp4_dequant_t(o["codes"], o["scales"], o["G"], 128, 512))
 
 
-@pytest.mark.parametrize("chunk", ["1", "2", "3"])
-@pytest.mark.parametrize("shape", [(7, 80, 336), (5, 64, 256), (4, 144, 528)])
-def test_lookahead_amax_chunks(nvq, oracle_mod, shape, chunk, monkeypatch):
-    """Slices quantised in chunks, each launch reducing the next chunk's amax
-    while it quantises the current one: outputs are those of the oracle."""
-    monkeypatch.setenv("NVQ_QUANT_CHUNK", chunk)
-    w = weights(shape, seed=300 + int(chunk) + sum(shape))
+@pytest.fixture
+def quant_lead(nvq):
+    """Sets the quantisers' look-ahead lead for one test, then restores 2."""
+    yield nvq.debug_set_quant_lead
+    nvq.debug_set_quant_lead(2)
+
+
+@pytest.mark.parametrize("lead", [2, 3, 6])
+@pytest.mark.parametrize("shape", [(7, 80, 336), (5, 64, 256), (4, 144, 528), (40, 64, 256),
+                                   (3, 1040, 96)])
+def test_single_pass_amax(nvq, oracle_mod, shape, lead, quant_lead):
+    """The slice amax is reduced inside the quantising pass from tiles loaded
+    one slice plus `lead` grid waves ahead (2: the least lead, the least
+    slack before a slice's amax is needed).  Ragged
+    row tiles (80, 144 and 1040 rows) load rows of the next slice, which the
+    look-ahead must leave out.  Outputs are those of the oracle."""
+    quant_lead(lead)
+    w = weights(shape, seed=300 + lead + sum(shape))
     wn = u16(w)
     for f46 in (False, True):
-        r = nvq.nvfp4_quantize_dual(w.cuda(), four_over_six=f46)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        r = nvq.nvfp4_quantize_dual(w.cuda(), four_over_six=f46, status=st)
         orow = oracle_mod.nvfp4_quantize(wn, four_over_six=f46)
         ocol = oracle_mod.nvfp4_quantize_colwise(wn, four_over_six=f46)
+        assert int(st.item()) == 0
         assert_same(f32(r["amax"]).view(np.uint32), orow["amax"].view(np.uint32), "amax")
         assert_same(f32(r["tensor_scale"]).view(np.uint32), orow["G"].view(np.uint32), "G")
         assert_same(u8(r["codes_row"]), orow["codes"], "codes_row")
         assert_same(u8(r["scales_row"]), orow["scales"], "scales_row")
         assert_same(u8(r["codes_col"]), ocol["codes"], "codes_col")
         assert_same(u8(r["scales_col"]), ocol["scales"], "scales_col")
-        r1 = nvq.nvfp4_quantize(w.cuda(), four_over_six=f46)
+        r1 = nvq.nvfp4_quantize(w.cuda(), four_over_six=f46, status=st)
+        assert int(st.item()) == 0
         assert_same(u8(r1["codes"]), orow["codes"], "rowwise-only codes")
+        assert_same(u8(r1["scales"]), orow["scales"], "rowwise-only scales")
+        assert_same(f32(r1["tensor_scale"]).view(np.uint32), orow["G"].view(np.uint32), "G")
 
 
-def test_misaligned_stack_falls_back(nvq, oracle_mod, monkeypatch):
-    """A stack that is 16- but not 32-byte aligned takes the separate amax pass."""
-    monkeypatch.setenv("NVQ_QUANT_CHUNK", "1")
+def test_slice_amax_outlier_in_last_ragged_rows(nvq, oracle_mod):
+    """An outlier in the last rows of a slice whose row count is not a
+    multiple of the 64-row tile: it must raise that slice's amax only."""
+    w = weights((3, 80, 256), seed=91)
+    w[1, 79, 200] = 50.0
+    w[0, 70, 3] = -40.0
+    wn = u16(w)
+    r = nvq.nvfp4_quantize_dual(w.cuda(), four_over_six=True)
+    o = oracle_mod.nvfp4_quantize(wn, four_over_six=True)
+    assert_same(f32(r["amax"]).view(np.uint32), o["amax"].view(np.uint32), "amax")
+    assert_same(u8(r["codes_row"]), o["codes"], "codes_row")
+
+
+def test_stack_16_byte_aligned(nvq, oracle_mod):
+    """A stack that is 16- but not 32-byte aligned (the copies need 16)."""
     w = weights((3, 64, 256), seed=77)
     buf = torch.empty(w.numel() + 8, dtype=torch.bfloat16, device="cuda")
     wv = buf[8:].view(3, 64, 256)
