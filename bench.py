@@ -26,7 +26,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -197,13 +196,47 @@ class ClockSampler:
 
 # ------------------------------------------------------------- the oracle
 
+def synth_module():
+    """The seeded input generators (synth.py), loaded from their file alone:
+    the CPU arms use them without importing the package, which loads the
+    CUDA library."""
+    import importlib.util
+    path = os.path.join(ROOT, "rl_nvfp4_quantize_gb300", "synth.py")
+    spec = importlib.util.spec_from_file_location("nvq_synth_standalone", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def host_info():
+    """The host the CPU baseline ran on: its logical CPUs and CPU model."""
+    import platform
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:  # lscpu missing: fall back to /proc/cpuinfo
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"host_cpus": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine(),
+            "machine": platform.machine()}
+
+
 def host_sample(frac, wl=None, seed_base=1):
     """Host (CPU) inputs for a proportional sample of the step: a fraction
     `frac` of the rows of each weight stack (taken from expert 0) and of the
     tokens of each activation tensor.  Taken from the device workload when
     given, else generated on the host with the same distributions."""
-    import torch
-    from rl_nvfp4_quantize_gb300 import synth
     r_gu = max(16, int(round(frac * GATE_UP[0] * GATE_UP[1])) // 16 * 16)
     r_dn = max(16, int(round(frac * DOWN[0] * DOWN[1])) // 16 * 16)
     assert r_gu <= GATE_UP[1] and r_dn <= DOWN[1], "sample larger than one expert"
@@ -213,6 +246,7 @@ def host_sample(frac, wl=None, seed_base=1):
         dn = wl.dn[0:1, :r_dn].cpu()
         xs = [wl.x[i][:t].cpu() for i, t in enumerate(toks)]
     else:
+        synth = synth_module()
         gu = synth.expert_weights(1, r_gu, GATE_UP[2], seed=seed_base + 1)
         dn = synth.expert_weights(1, r_dn, DOWN[2], seed=seed_base + 2)
         xs = [synth.activations(t, H, seed=seed_base + 3 + i) for i, (t, (_, H)) in enumerate(zip(toks, ACTS))]
@@ -285,8 +319,9 @@ def run_reference(args):
             "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample_fraction": frac},
-            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": "%s per step (fraction %g of the step)" % (desc, frac)},
+            "cpu_baseline": dict({"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": "%s per step (fraction %g of the step)" % (desc, frac)},
+                                 **host_info()),
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -373,6 +408,11 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.experts != 256:
         set_experts(args.experts)
+    if args.impl == "reference":
+        # the CPU oracle alone: the product's CUDA library is neither built
+        # nor loaded on this arm
+        run_reference(args)
+        return
     if args.case:
         import __graft_entry__
         __graft_entry__.build()
@@ -381,9 +421,6 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    if args.impl == "reference":
-        run_reference(args)
-        return
 
     import torch
     import rl_nvfp4_quantize_gb300 as nvq  # noqa: F401
@@ -454,7 +491,7 @@ def main():
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(wl, calls, max(2, min(args.steps, 5)), stream, world)
+        e2e = measure_e2e(wl, calls, 10, stream, world)
 
     context = None
     if not args.no_context:
@@ -468,6 +505,7 @@ def main():
                          % (desc, args.cpu_frac, sec),
                "elem_per_s": round(el / sec, 1),
                "extrapolated_step_s": round(step_bytes / (b / sec), 1)}
+        cpu.update(host_info())
 
     traffic = load_traffic(dom[0])
     issue = issue_view(dom[0], dom[1], GATE_UP if "gate_up" in dom[0] else DOWN)
@@ -969,20 +1007,28 @@ def measure_e2e(wl, calls, steps, stream, world):
     one()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    streams = (stream, s_in, s_in2, s_out)
+    # the end of every step on every stream: step i ends when its last
+    # stream does (steps overlap across streams, so a step's time is the
+    # distance between consecutive step ends)
+    ends = [[torch.cuda.Event(enable_timing=True) for _ in streams] for _ in range(steps)]
     barrier(world)
     a.record(stream)
     for si in (s_in, s_in2, s_out):
         si.wait_event(a)
-    for _ in range(steps):
+    for i in range(steps):
         one()
-    for e, s in zip(ends, (stream, s_in, s_in2, s_out)):
-        e.record(s)
+        for e, s in zip(ends[i], streams):
+            e.record(s)
     torch.cuda.synchronize()
-    el = max_over_ranks(world, max(a.elapsed_time(e) for e in ends) / 1e3)
+    end_ms = [max(a.elapsed_time(e) for e in row) for row in ends]
+    per_step = sorted([end_ms[0]] + [end_ms[i] - end_ms[i - 1] for i in range(1, steps)])
+    el = max_over_ranks(world, end_ms[-1] / 1e3)
     return {"value": round(job_rate(world, step_bytes, steps, el), 3), "unit": "GB/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "ms_per_step": round(1e3 * el / steps, 3),
+            "steps": steps, "ms_per_step": round(1e3 * el / steps, 3),
+            "ms_per_step_median": round(per_step[len(per_step) // 2], 3),
+            "ms_per_step_min": round(per_step[0], 3), "ms_per_step_max": round(per_step[-1], 3),
             "overlap": "host-to-device copies (two streams), kernels and device-to-host copies"}
 
 
