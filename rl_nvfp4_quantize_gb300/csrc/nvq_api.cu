@@ -77,20 +77,6 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
-                    uint64_t dim0, uint64_t dim1, uint64_t dim2, uint64_t stride1,
-                    uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2,
-                    CUtensorMapSwizzle swizzle) {
-  if (!get_encode()) return false;
-  const cuuint64_t dims[3] = {dim0, dim1, dim2};
-  const cuuint64_t strides[2] = {stride1, stride2};
-  const cuuint32_t box[3] = {box0, box1, box2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // ------------------------------------------------------------ debug kernels
 __global__ void k_debug_convert(int kind, const void* in, void* out, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;

@@ -608,25 +608,6 @@ __device__ __forceinline__ bool wait_done(const uint32_t* p, uint32_t& w,
   return false;
 }
 
-// 3-D tiled TMA store of one box (coordinates non-negative; parts of the box
-// outside the tensor are not written).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
-                                             const void* smem_src) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
-      "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until at most N committed bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
 // Orders generic-proxy shared-memory writes before later TMA reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -64,13 +64,6 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint64_t dim0, uint64_t dim1, uint64_t stride_bytes, uint32_t box0,
                     uint32_t box1, CUtensorMapSwizzle swizzle);
 
-// 3-D variant: [dim2][dim1][dim0], pitches stride1 (between dim1 rows) and
-// stride2 (between dim2 slices) in bytes.
-bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
-                    uint64_t dim0, uint64_t dim1, uint64_t dim2, uint64_t stride1,
-                    uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2,
-                    CUtensorMapSwizzle swizzle);
-
 struct DevInfo {
   int sms;
   int ok;  // 1 when the device is compute capability 10.3

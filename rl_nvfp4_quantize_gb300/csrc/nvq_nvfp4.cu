@@ -999,160 +999,87 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
 // ------------------------------------------------------- transposed dequant
 // Tiles of 128 out-rows x 256 in-columns of the rowwise copy.  Thread
 // (g = tid & 15, b = tid >> 4) dequantises out-rows 8g .. 8g+7 of 16-wide
-// block column b and writes them, transposed, as 16-byte runs into a shared
-// [in][out] tile laid out as two 128-byte-swizzled TMA boxes of 64 out-rows
-// (chunk c of tile row r at c ^ (r & 7)): the eight lanes of each store
-// phase hit eight different chunks.  One thread then stores the two boxes
-// with TMA into the [nexp, in, out] result (a 3-D map, so a ragged tile never
-// spills into the next slice).  The next tile's codes are loaded into
-// registers while the stores drain.  Each column pair of a thread's block is
-// dequantised and written to shared memory before the next, so no 8 x 8
-// output block is held in registers.  Two CTAs per SM: with a third, L1
-// shrinks to about a third and the row-strided code loads, whose 32-byte
-// sectors other warps finish using, miss it (measured 47 % slower).
-#ifndef NVQ_TQ_MINB
-#define NVQ_TQ_MINB 2
-#endif
-constexpr int kTqR = 128, kTqC = 256, kTqThreads = 256;
-constexpr int kTqBox = kTqC * 64 * 2;                                  // 32 KiB per box
-constexpr int kTqSmem = 2 * kTqBox + kScaleTableBytes;                  // 64 KiB tile + table
+// block column b and writes each of its 16 in-columns straight to global
+// memory as one 16-byte run of an output row: the 16 lanes of a warp that
+// share a block column write 16 x 16 contiguous bytes of one row of the
+// [nexp, in, out] result, so a warp store is two full 256-byte runs and no
+// shared staging, fence, barrier or TMA store is needed.  Consecutive tiles
+// step along `out` first, so the CTAs running together fill neighbouring
+// pieces of the same output rows.  Measured alternatives: staging the tile
+// in shared memory and storing it with TMA boxes was the same speed (2 %
+// slower on the down stack); taller tiles (256 or 512 out-rows, longer
+// contiguous output per row) and one block column per warp (512-byte
+// stores) were 15-35 % slower, as were three or four CTAs per SM: the
+// row-strided code loads rely on L1 keeping the 32-byte sectors that the
+// neighbouring warp also reads.
+constexpr int kTqThreads = 256;
 
-// Column pair J (block columns 2J, 2J+1) of this thread's eight out-rows:
-// dequantised and written as two 16-byte runs of the shared [in][out] tile.
-template <int J>
-__device__ __forceinline__ void dqt_column_pair(const uint2 cw[8], const uint32_t S2[8], float2 G2,
-                                                unsigned char* box, int b, int g) {
-  uint32_t v[8];  // bf16 pair (columns 2J, 2J+1) of row i
-#pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const uint32_t h = e2m1x2_dec_byte<J & 3>(J < 4 ? cw[i].x : cw[i].y);
-    const float2 y = __fmul2_rn(cs_exact(h, S2[i]), G2);
-    v[i] = bf16x2_rn(y.x, y.y);
-  }
-  const int r = b * 16 + 2 * J;  // tile row (in-index) of column 2J
-  const int off0 = r * 128 + (((g & 7) ^ (r & 7)) << 4);
-  const int off1 = (r + 1) * 128 + (((g & 7) ^ ((r + 1) & 7)) << 4);
-  *reinterpret_cast<uint4*>(box + off0) =
-      make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
-                 __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410));
-  *reinterpret_cast<uint4*>(box + off1) =
-      make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632),
-                 __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632));
-}
-
-struct DequantTArgs {  // aligned as CUtensorMap requires
-  CUtensorMap tmap;  // dst as [nexp][in][out] bf16, boxes of 64 x 256 x 1
-  const uint8_t* codes;
-  const uint8_t* scales;
-  const float* G;
-  int out, in;
-  FastDiv per_exp, by_tiles_r;
-  uint32_t ntiles;
-};
-
-__global__ void __launch_bounds__(kTqThreads, NVQ_TQ_MINB) k_dequant_t(const __grid_constant__ DequantTArgs A) {
-  extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* const tile = smem;
-  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(smem + 2 * kTqBox);
+__global__ void __launch_bounds__(kTqThreads, 2)
+    k_dequant_t(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                const float* __restrict__ G, int out, int in, FastDiv per_exp, FastDiv by_tiles_r,
+                uint32_t ntiles, uint16_t* __restrict__ dst) {
+  __shared__ ScaleEnt tbl[128];
   build_scale_table(tbl);
+  __syncthreads();
   const int tid = threadIdx.x;
   const int g = tid & 15, b = tid >> 4;
-  const int out = A.out, in = A.in;
   const int64_t in_h = in >> 1, in_16 = in >> 4;
-  unsigned char* const box = tile + (g >> 3) * kTqBox;
-
-  // Consecutive tiles step along `out` first: the CTAs running at the same
-  // time then fill neighbouring 256-byte pieces of the same rows of the
-  // transposed result.
-  struct Tile { uint32_t e; int r0, c0, rv, cv; };
-  auto tile_of = [&](uint32_t t) {
-    Tile T;
-    T.e = A.per_exp.div(t);
-    const uint32_t rem = t - T.e * A.per_exp.d;
-    const int tc = (int)A.by_tiles_r.div(rem), tr = (int)(rem - tc * A.by_tiles_r.d);
-    T.r0 = tr * kTqR;
-    T.c0 = tc * kTqC;
-    T.rv = min(kTqR, out - T.r0);
-    T.cv = min(kTqC, in - T.c0);
-    return T;
-  };
-  uint2 cw[8];
-  uint32_t sb[8];
-  auto load = [&](uint32_t t) {
-    const Tile T = tile_of(t);
-    const bool ok = g * 8 < T.rv && b * 16 < T.cv;
-    const int64_t grow = (int64_t)T.e * out + T.r0 + g * 8;
-    const uint8_t* pc = A.codes + grow * in_h + (T.c0 >> 1) + b * 8;
-    const uint8_t* ps = A.scales + grow * in_16 + (T.c0 >> 4) + b;
+  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const uint32_t e = per_exp.div(t);
+    const uint32_t rem = t - e * per_exp.d;
+    const int tc = (int)by_tiles_r.div(rem), tr = (int)(rem - tc * by_tiles_r.d);
+    const int r0 = tr * 128, c0 = tc * 256;
+    if (g * 8 >= min(128, out - r0) || b * 16 >= min(256, in - c0)) continue;
+    const int64_t grow = (int64_t)e * out + r0 + g * 8;
+    const uint8_t* pc = codes + grow * in_h + (c0 >> 1) + b * 8;
+    const uint8_t* ps = scales + grow * in_16 + (c0 >> 4) + b;
+    uint2 cw[8];
+    uint32_t S2[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-      cw[i] = ok ? __ldg(reinterpret_cast<const uint2*>(pc + i * in_h)) : make_uint2(0, 0);
-      sb[i] = ok ? __ldg(ps + i * in_16) : 0u;
+      cw[i] = __ldg(reinterpret_cast<const uint2*>(pc + i * in_h));
+      S2[i] = __ldg(ps + i * in_16);
     }
-  };
-
-  if (smem_u32(smem) & 1023u) return;  // the swizzled boxes need a 1 KiB aligned base
-  if (blockIdx.x < A.ntiles) load(blockIdx.x);
-  for (uint32_t t = blockIdx.x; t < A.ntiles; t += gridDim.x) {
-    if (tid == 0) bulk_wait_read<0>();  // the previous tile's stores have read the tile
-    __syncthreads();
-    const Tile T = tile_of(t);
-    const float Gv = A.G[T.e];
-    const float2 G2 = make_float2(Gv, Gv);
-    if (g * 8 < T.rv && b * 16 < T.cv) {
-      uint32_t S2[8];
 #pragma unroll
-      for (int i = 0; i < 8; i++) S2[i] = pos_s2(tbl[sb[i] & 0x7f]);
-      dqt_column_pair<0>(cw, S2, G2, box, b, g);
-      dqt_column_pair<1>(cw, S2, G2, box, b, g);
-      dqt_column_pair<2>(cw, S2, G2, box, b, g);
-      dqt_column_pair<3>(cw, S2, G2, box, b, g);
-      dqt_column_pair<4>(cw, S2, G2, box, b, g);
-      dqt_column_pair<5>(cw, S2, G2, box, b, g);
-      dqt_column_pair<6>(cw, S2, G2, box, b, g);
-      dqt_column_pair<7>(cw, S2, G2, box, b, g);
+    for (int i = 0; i < 8; i++) S2[i] = pos_s2(tbl[S2[i] & 0x7f]);
+    const float Gv = G[e];
+    const float2 G2 = make_float2(Gv, Gv);
+    // output row (in-index) c0 + 16b + j, out-columns r0 + 8g .. +7
+    uint16_t* const d0 = dst + ((int64_t)e * in + c0 + 16 * b) * out + r0 + 8 * g;
+#pragma unroll
+    for (int J = 0; J < 8; J++) {
+      uint32_t v[8];  // bf16 pair (in-columns 2J, 2J+1) of out-row i
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const uint32_t word = J < 4 ? cw[i].x : cw[i].y;
+        const uint32_t h = e2m1x2_dec(__byte_perm(word, 0, 0x4440 + (J & 3)));
+        const float2 y = __fmul2_rn(cs_exact(h, S2[i]), G2);
+        v[i] = bf16x2_rn(y.x, y.y);
+      }
+      stg_stream(d0 + (int64_t)(2 * J) * out,
+                 make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                            __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410)));
+      stg_stream(d0 + (int64_t)(2 * J + 1) * out,
+                 make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632),
+                            __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632)));
     }
-    fence_proxy_async_smem();  // make this thread's tile writes visible to the TMA unit
-    __syncthreads();
-    if (tid == 0) {
-      tma_store_3d(&A.tmap, T.r0, T.c0, (int)T.e, tile);
-      if (T.rv > 64) tma_store_3d(&A.tmap, T.r0 + 64, T.c0, (int)T.e, tile + kTqBox);
-      bulk_commit();
-    }
-    if (t + gridDim.x < A.ntiles) load(t + gridDim.x);
   }
-  if (tid == 0) bulk_wait<0>();
 }
 
 cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const float* G,
                              int64_t nexp, int out, int in, uint16_t* dst, cudaStream_t s) {
-  static PerDeviceOnce attr;
-  const cudaError_t err0 = attr.run([] {
-    return cudaFuncSetAttribute(k_dequant_t, cudaFuncAttributeMaxDynamicSharedMemorySize, kTqSmem);
-  });
-  if (err0 != cudaSuccess) return err0;
   const DevInfo* di = device_info();
-  const int tiles_r = (out + kTqR - 1) / kTqR, tiles_c = (in + kTqC - 1) / kTqC;
+  const int tiles_r = (out + 127) / 128, tiles_c = (in + 255) / 256;
   const int64_t ntiles = nexp * tiles_r * tiles_c;
   if (ntiles == 0) return cudaSuccess;
-  if (ntiles >= (1ll << 31) - (1ll << 24) || nexp >= (1ll << 31)) return cudaErrorInvalidValue;
-  DequantTArgs A;
-  if (!encode_tmap_3d(&A.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, dst, (uint64_t)out, (uint64_t)in,
-                      (uint64_t)nexp, (uint64_t)out * 2, (uint64_t)out * in * 2, 64, kTqC, 1,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  A.codes = codes;
-  A.scales = scales;
-  A.G = G;
-  A.out = out;
-  A.in = in;
-  A.per_exp.d = (uint32_t)(tiles_r * tiles_c);
-  make_fastdiv(A.per_exp.d, &A.per_exp.m, &A.per_exp.s);
-  A.by_tiles_r.d = (uint32_t)tiles_r;
-  make_fastdiv(A.by_tiles_r.d, &A.by_tiles_r.m, &A.by_tiles_r.s);
-  A.ntiles = (uint32_t)ntiles;
-  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * NVQ_TQ_MINB);
-  k_dequant_t<<<grid, kTqThreads, kTqSmem, s>>>(A);
+  if (ntiles >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
+  FastDiv pe, br;
+  pe.d = (uint32_t)(tiles_r * tiles_c);
+  make_fastdiv(pe.d, &pe.m, &pe.s);
+  br.d = (uint32_t)tiles_r;
+  make_fastdiv(br.d, &br.m, &br.s);
+  const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * 2);
+  k_dequant_t<<<grid, kTqThreads, 0, s>>>(codes, scales, G, out, in, pe, br, (uint32_t)ntiles, dst);
   return cudaGetLastError();
 }
 

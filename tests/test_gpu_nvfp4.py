@@ -292,3 +292,20 @@ def test_codes_col_16_byte_aligned(nvq, oracle_mod):
     ocol = oracle_mod.nvfp4_quantize_colwise(u16(w), four_over_six=True)
     assert_same(u8(cc), ocol["codes"], "codes_col")
     assert_same(u8(r["scales_col"]), ocol["scales"], "scales_col")
+
+
+@pytest.mark.parametrize("shape", [(1, 16, 16), (2, 80, 96), (3, 528, 272), (2, 1040, 64),
+                                   (1, 512, 1024), (2, 1536, 144)])
+def test_transposed_dequant_ragged_tiles(nvq, oracle_mod, shape):
+    """The transposed dequant over shapes ragged against its 128 x 256 tiles
+    (out and in not multiples of the tile, slices smaller than a tile):
+    same bytes as the oracle, guard bands intact."""
+    w = weights(shape, seed=4000 + sum(shape))
+    E, R, K = shape
+    r = nvq.nvfp4_quantize(w.cuda(), four_over_six=True)
+    gt = Guarded((E, K, R), torch.bfloat16)
+    dt = nvq.nvfp4_dequant_t(r["codes"], r["scales"], r["tensor_scale"], out=gt.t)
+    torch.cuda.synchronize()
+    assert gt.intact()
+    codes, scales, G = u8(r["codes"]), u8(r["scales"]), f32(r["tensor_scale"])
+    assert_same(u16(dt), oracle_mod.nvfp4_dequant_t(codes, scales, G, R, K), "dequant_t")
