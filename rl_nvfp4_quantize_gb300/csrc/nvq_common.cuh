@@ -530,6 +530,18 @@ __device__ __forceinline__ bool named_barrier_or(int id, int n, bool pred) {
   return r != 0;
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`, with an L2
+// eviction policy.
+__device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled TMA load of one box at element coordinates (x, y) into shared
 // memory, completing on `bar` (x * element size must be a multiple of 16).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,

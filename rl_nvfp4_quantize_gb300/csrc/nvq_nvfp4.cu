@@ -730,8 +730,13 @@ cudaError_t launch_quant_tiles(const uint16_t* w, int64_t nexp, int rows, int co
 }
 
 // ------------------------------------------------------ per-token activations
-// One CTA of 128 threads per token row.  Up to kActRegBlocks blocks per
-// thread stay in registers between the row-amax reduction and the
+// Three kernels by row length H: rows of at most 2048 values take one warp
+// per token with the row in registers (k_act_warp); rows up to
+// kActStreamMaxH values one warp per token streaming rows through shared
+// memory (k_act_stream); longer rows one CTA per token (k_act).
+//
+// k_act: one CTA of 128 threads per token row.  Up to kActRegBlocks blocks
+// per thread stay in registers between the row-amax reduction and the
 // quantisation; longer rows re-read the remaining blocks (from cache).
 constexpr int kActThreads = 128;
 constexpr int kActRegBlocks = 4;
@@ -891,6 +896,122 @@ __global__ void __launch_bounds__(kActWarpThreads)
   }
 }
 
+// Longer rows of up to kActStreamMaxH values take one warp per token row, and
+// each warp streams its rows (w, w + W, w + 2W, ... of the grid's W warps)
+// through its own ring of S shared-memory row buffers filled by 1-D bulk
+// copies (L2 evict-first), so many rows are in flight per SM without
+// holding them in registers.  From a staged row the warp takes the row
+// amax (any chunk order, one pass), then quantises block b = lane + 32k
+// from its 32 bytes in a second pass.  16 warps per CTA, one CTA per SM;
+// S = as many buffers as fit 200 KiB.
+constexpr int kActStreamThreads = 512;
+constexpr int kActStreamWarps = kActStreamThreads / 32;
+constexpr int kActStreamBytes = 200 * 1024;
+constexpr int kActStreamMaxH = kActStreamBytes / (kActStreamWarps * 2);  // S >= 1
+constexpr int kActStreamMaxS = 8;
+
+__host__ __device__ constexpr int act_stream_stages(int H) {
+  return (kActStreamBytes / (kActStreamWarps * 2 * H)) < kActStreamMaxS
+             ? kActStreamBytes / (kActStreamWarps * 2 * H)
+             : kActStreamMaxS;
+}
+__host__ __device__ constexpr int act_stream_smem(int H) {
+  return kActStreamWarps * act_stream_stages(H) * 2 * H + kActStreamWarps * kActStreamMaxS * 8 +
+         kScaleTableBytes;
+}
+
+template <bool F46>
+__global__ void __launch_bounds__(kActStreamThreads, 1)
+    k_act_stream(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
+                 uint8_t* __restrict__ scales, float* __restrict__ token_scale,
+                 int* __restrict__ status, int tiled) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int S = act_stream_stages(H);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rowbytes = 2u * (uint32_t)H;
+  unsigned char* const ring = smem + (size_t)warp * S * rowbytes;
+  uint64_t* const bar = reinterpret_cast<uint64_t*>(smem + (size_t)kActStreamWarps * S * rowbytes) +
+                        warp * kActStreamMaxS;
+  ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(
+      smem + (size_t)kActStreamWarps * S * rowbytes + kActStreamWarps * kActStreamMaxS * 8);
+  build_scale_table(tbl);
+  if (lane == 0) {
+    for (int i = 0; i < S; i++) mbar_init(&bar[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int nb = H / 16;
+  const int ct = (nb + 3) / 4;  // tiled layout: tiles per tile row
+  const float six_m = F46 ? 1536.0f : 2688.0f;
+  const int64_t W = (int64_t)gridDim.x * kActStreamWarps;
+  const int64_t w0 = (int64_t)blockIdx.x * kActStreamWarps + warp;
+  uint64_t pol = 0;
+  if (lane == 0) pol = l2_policy_evict_first();
+  auto issue = [&](int64_t j) {  // lane 0: the warp's j-th row into stage j % S
+    const int64_t row = w0 + j * W;
+    if (row < T) {
+      uint64_t* b = &bar[j % S];
+      mbar_arrive_expect_tx(b, rowbytes);
+      bulk_load_hint(ring + (j % S) * rowbytes, x + row * H, rowbytes, b, pol);
+    }
+  };
+  if (lane == 0)
+    for (int j = 0; j < S; j++) issue(j);
+  for (int64_t j = 0; w0 + j * W < T; j++) {
+    const int64_t row = w0 + j * W;
+    const unsigned char* buf = ring + (j % S) * rowbytes;
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar[j % S], (uint32_t)(j / S) & 1, 1u << 22))) {
+      // a copy never landed: report and stop, after the copies in flight
+      if (lane == 0) {
+        if (status) atomicOr(status, kStatusTimeout);
+        for (int64_t i = j + 1; i < j + S && w0 + i * W < T; i++)
+          mbar_wait(&bar[i % S], (uint32_t)(i / S) & 1, 1u << 22);
+      }
+      return;
+    }
+    // row amax: magnitude maximum on bf16 bit patterns (exact; NaN above
+    // inf), four independent chains
+    uint32_t m4[4] = {0, 0, 0, 0};
+#pragma unroll 4
+    for (int c = lane; c < (int)(rowbytes >> 4); c += 32) {
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + c * 16);
+      m4[0] = umaxmag2(m4[0], v.x);
+      m4[1] = umaxmag2(m4[1], v.y);
+      m4[2] = umaxmag2(m4[2], v.z);
+      m4[3] = umaxmag2(m4[3], v.w);
+    }
+    const uint32_t m = umaxmag2(umaxmag2(m4[0], m4[1]), umaxmag2(m4[2], m4[3]));
+    uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
+    mm = __reduce_max_sync(0xffffffffu, mm);
+    const float am = __uint_as_float(mm);
+    float G, E;
+    global_scales(am, six_m, G, E);
+    if (lane == 0) {
+      token_scale[row] = G;
+      if (status && !isfinite(am)) atomicOr(status, kStatusNonFinite);
+    }
+    // blocks lane + 32k, four at a time so that their chains interleave
+    for (int b0 = lane; b0 < nb; b0 += 128) {
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int b = b0 + 32 * k;
+        if (b < nb) {
+          const uint4 lo = *reinterpret_cast<const uint4*>(buf + b * 32);
+          const uint4 hi = *reinterpret_cast<const uint4*>(buf + b * 32 + 16);
+          const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          uint32_t c0w, c1w, sb;
+          quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
+          stg_stream_v2(codes + row * (H / 2) + b * 8, c0w, c1w);
+          if (tiled) scales[scale_off_tiled(row, b, ct)] = (uint8_t)sb;
+          else stg_stream_u8(scales + row * nb + b, sb);
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with the buffer before it is refilled
+    if (lane == 0) issue(j + S);
+  }
+}
+
 cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* codes,
                        uint8_t* scales, float* token_scale, int* status, bool tiled,
                        cudaStream_t s) {
@@ -915,6 +1036,30 @@ cudaError_t launch_act(const uint16_t* x, int64_t T, int H, bool f46, uint8_t* c
       k_act_warp<true><<<g, kActWarpThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
     else
       k_act_warp<false><<<g, kActWarpThreads, 0, s>>>(x, T, H, codes, scales, token_scale, status, t);
+    return cudaGetLastError();
+  }
+  if (H <= kActStreamMaxH) {
+    const int smem = act_stream_smem(H);
+    static PerDeviceOnce attr[2];
+    cudaError_t err = attr[f46].run([] {
+      cudaError_t e = cudaFuncSetAttribute(k_act_stream<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kActStreamBytes + kActStreamWarps * kActStreamMaxS * 8 +
+                                               kScaleTableBytes);
+      if (e != cudaSuccess) return e;
+      return cudaFuncSetAttribute(k_act_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kActStreamBytes + kActStreamWarps * kActStreamMaxS * 8 +
+                                      kScaleTableBytes);
+    });
+    if (err != cudaSuccess) return err;
+    const int64_t need = (T + kActStreamWarps - 1) / kActStreamWarps;
+    const int g = (int)std::min<int64_t>(need, (int64_t)di->sms);
+    if (f46)
+      k_act_stream<true><<<g, kActStreamThreads, smem, s>>>(x, T, H, codes, scales, token_scale,
+                                                            status, t);
+    else
+      k_act_stream<false><<<g, kActStreamThreads, smem, s>>>(x, T, H, codes, scales, token_scale,
+                                                             status, t);
     return cudaGetLastError();
   }
   const int grid = (int)std::min<int64_t>(T, (int64_t)di->sms * 16);

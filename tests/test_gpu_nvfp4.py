@@ -309,3 +309,19 @@ def test_transposed_dequant_ragged_tiles(nvq, oracle_mod, shape):
     assert gt.intact()
     codes, scales, G = u8(r["codes"]), u8(r["scales"]), f32(r["tensor_scale"])
     assert_same(u16(dt), oracle_mod.nvfp4_dequant_t(codes, scales, G, R, K), "dequant_t")
+
+
+@pytest.mark.parametrize("T,H", [(8000, 2064), (2500, 6400), (4097, 6144), (300, 2080)])
+def test_act_streamed_rows_wrap_the_ring(nvq, oracle_mod, T, H):
+    """Rows of 2048 < H <= 6400 values stream through each warp's ring of
+    row buffers; with more rows per warp than buffers the ring wraps (its
+    barriers change phase): same bytes as the oracle."""
+    from rl_nvfp4_quantize_gb300 import synth
+    x = synth.activations(T, H, seed=T + H)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = nvq.act_quantize_per_token(x.cuda(), four_over_six=True, status=st)
+    o = oracle_mod.act_quantize_per_token(u16(x), four_over_six=True)
+    assert int(st.item()) == 0
+    assert_same(u8(r["codes"]), o["codes"], "codes")
+    assert_same(u8(r["scales"]), o["scales"], "scales")
+    assert_same(f32(r["token_scale"]).view(np.uint32), o["token_scale"].view(np.uint32), "token_scale")
