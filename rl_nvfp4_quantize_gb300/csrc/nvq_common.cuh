@@ -106,14 +106,6 @@ __device__ __forceinline__ float div6(float a) {
   return __fmaf_rn(r, y, q0);
 }
 
-__device__ __forceinline__ float2 div6x2(float2 a) {
-  const float2 y = make_float2(0x1.555556p-3f, 0x1.555556p-3f);
-  const float2 m6 = make_float2(-6.0f, -6.0f);
-  float2 q0 = __fmul2_rn(a, y);
-  float2 r = __ffma2_rn(q0, m6, a);
-  return __ffma2_rn(r, y, q0);
-}
-
 // Two FP32 values -> two E4M3 bytes (RNE, saturating at 448).  Byte 0 of the
 // result encodes `lo`, byte 1 encodes `hi`.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -345,77 +337,6 @@ __device__ __forceinline__ void quant_row_block(const uint32_t w[8], float E, co
   const uint32_t m = maxabs2(maxabs2(maxabs2(w[0], w[1]), maxabs2(w[2], w[3])),
                              maxabs2(maxabs2(w[4], w[5]), maxabs2(w[6], w[7])));
   quant_row_block_amax<F46>(w, amax_fold(m), E, tbl, c0, c1, sb);
-}
-
-// Candidate of two columnwise blocks side by side (columns j and j+1):
-// u[i] = (t_ij, t_i,j+1) for the 16 rows i of the block.  Codes of column j
-// go to cj and of column j+1 to ck, each packed along the block (element 2k
-// in the low nibble of byte k).  Returns both errors, each accumulated as
-// an even-position and an odd-position chain added at the end.
-__device__ __forceinline__ float2 col_candidate(const float2 u[16], const ScaleEnt sj,
-                                                const ScaleEnt sk, uint32_t cj[2],
-                                                uint32_t ck[2]) {
-  const float2 r2 = make_float2(sj.rcp, sk.rcp);
-  float2 q[16];
-#pragma unroll
-  for (int i = 0; i < 16; i++) q[i] = __fmul2_rn(u[i], r2);
-  uint32_t hj[8], hk[8];
-  cj[0] = e2m1x8_enc_dec(q[0].x, q[1].x, q[2].x, q[3].x, q[4].x, q[5].x, q[6].x, q[7].x, hj);
-  cj[1] = e2m1x8_enc_dec(q[8].x, q[9].x, q[10].x, q[11].x, q[12].x, q[13].x, q[14].x, q[15].x,
-                         hj + 4);
-  ck[0] = e2m1x8_enc_dec(q[0].y, q[1].y, q[2].y, q[3].y, q[4].y, q[5].y, q[6].y, q[7].y, hk);
-  ck[1] = e2m1x8_enc_dec(q[8].y, q[9].y, q[10].y, q[11].y, q[12].y, q[13].y, q[14].y, q[15].y,
-                         hk + 4);
-  float2 accE = make_float2(0.0f, 0.0f), accO = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int k = 0; k < 8; k++) {
-    const float2 dj = resid2(hj[k], sj.negS2, u[2 * k].x, u[2 * k + 1].x);
-    const float2 dk = resid2(hk[k], sk.negS2, u[2 * k].y, u[2 * k + 1].y);
-    const float2 de = make_float2(dj.x, dk.x), dod = make_float2(dj.y, dk.y);
-    accE = __ffma2_rn(de, de, accE);
-    accO = __ffma2_rn(dod, dod, accO);
-  }
-  return __fadd2_rn(accE, accO);
-}
-
-// Quantises the two columnwise blocks held in 16 words wc[i] (row i of the
-// block; low half = column j, high half = column j+1).
-template <bool F46>
-__device__ __forceinline__ void quant_col_pair(const uint32_t wc[16], float E, const ScaleEnt* tbl,
-                                               uint32_t cj[2], uint32_t ck[2], uint32_t& sbj,
-                                               uint32_t& sbk) {
-  uint32_t m = maxabs2(wc[0], wc[1]);
-#pragma unroll
-  for (int i = 2; i < 16; i++) m = maxabs2(m, wc[i]);
-  m &= 0x7fff7fffu;
-  const float2 E2 = make_float2(E, E);
-  const float2 a = __fmul2_rn(make_float2(lo_f(m), hi_f(m)), E2);
-  const float2 a6 = div6x2(a);
-  const float2 a4 = __fmul2_rn(a, make_float2(0.25f, 0.25f));
-  const uint32_t s6 = e4m3x2(a6.x, a6.y);  // byte 0: column j, byte 1: column j+1
-  const uint32_t s4 = e4m3x2(a4.x, a4.y);
-  float2 u[16];
-#pragma unroll
-  for (int i = 0; i < 16; i++) u[i] = __fmul2_rn(widen2(wc[i]), E2);
-  const uint32_t s6j = s6 & 0x7fu, s6k = (s6 >> 8) & 0x7fu;
-  const float2 e6 = col_candidate(u, tbl[s6j], tbl[s6k], cj, ck);
-  sbj = s6j;
-  sbk = s6k;
-  if (F46) {
-    const uint32_t s4j = s4 & 0x7fu, s4k = (s4 >> 8) & 0x7fu;
-    uint32_t dj[2], dk[2];
-    const float2 e4 = col_candidate(u, tbl[s4j], tbl[s4k], dj, dk);
-    if (e4.x < e6.x) {
-      cj[0] = dj[0];
-      cj[1] = dj[1];
-      sbj = s4j;
-    }
-    if (e4.y < e6.y) {
-      ck[0] = dk[0];
-      ck[1] = dk[1];
-      sbk = s4k;
-    }
-  }
 }
 
 // ------------------------------------------------------- tiled scale layout

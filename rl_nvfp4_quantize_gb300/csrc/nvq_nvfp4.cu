@@ -64,18 +64,23 @@ cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q) {
 // One co-resident grid (cooperative launch), one CTA per SM, walks the
 // tiles of the whole stack -- 64 rows x 256 columns of one slice each --
 // in one global order g = slice * P + tile (P tiles per slice).  Each CTA
-// has two compute groups of eight warps and one control warp:
+// has two compute groups of eight warps, one control warp per group and a
+// look-ahead stream of two warps:
 //   * compute group k of CTA b (group index q = 2b + k of Gq = 2 * grid)
 //     quantises tiles q, q + Gq, q + 2Gq, ... from a two-stage ring.  It
 //     waits only on the stage's `full` barrier, which completes when the
-//     copy has landed and the control warp has placed the tile's slice
+//     copy has landed and its control warp has placed the tile's slice
 //     encode factor E beside it, and releases the stage on its `empty`
 //     barrier.  It never waits on the rest of the grid.
-//   * the control warp issues every copy, and computes the slice amax in
-//     the same pass over the stack (S1): it streams this CTA's look-ahead
-//     tiles (the same tile indices as its two groups, up to L tiles ahead
-//     of them) through a two-stage ring, reduces each to its magnitude
-//     maximum, and keeps the per-slice results described below.
+//   * control warp k issues group k's copies in order, each once its stage
+//     is released, and gives each tile its E once the slice is finished.
+//     It spends its time blocked in barrier waits, not polling, so the
+//     compute warps keep the issue slots.
+//   * the look-ahead stream computes the slice amax in the same pass over
+//     the stack (S1): it streams this CTA's look-ahead tiles (the same tile
+//     indices as its two groups, up to L tiles ahead of them) through a
+//     small ring, reduces each to its magnitude maximum, and keeps the
+//     per-slice results described below.
 // The look-ahead copies use the L2 evict-last policy and the quantising
 // copies (the same bytes, later) evict-first: the look-ahead read is the
 // HBM read, the second read hits L2, which holds the window of about L
@@ -83,7 +88,7 @@ cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q) {
 //
 // Per slice s, word ts[s] (the tensor_scale output, zeroed first) counts
 // the look-ahead tiles reduced so far, until it holds the slice's result.
-// The control warp folds each tile's maximum into amax[s] with an atomic
+// The look-ahead stream folds each tile's maximum into amax[s] with an atomic
 // max at once and adds its CTA's tile count for a slice to ts[s] in one
 // release add when its look-ahead moves on to the next slice (by then its
 // earlier atomics have completed, so the release costs little).  The CTA
@@ -106,9 +111,9 @@ cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q) {
 //   rowwise pass   : 1024 blocks of 1x16, four per thread, results stored
 //                    straight to global (8 code bytes + 1 scale byte);
 //   columnwise pass: 256 units of 16 rows x 4 columns, one per thread, each
-//                    column pair processed with packed f32x2 arithmetic; the
-//                    results are staged and written as contiguous runs of the
-//                    transposed [in, out/2] layout.
+//                    column regrouped into the pair layout of a rowwise block
+//                    and quantised as one; the results are staged and written
+//                    as contiguous runs of the transposed [in, out/2] layout.
 // Inside a swizzled box, 16-byte chunk c of row r sits at chunk c ^ (r & 7).
 constexpr int kTR = 64, kTC = 256;
 constexpr int kBoxC = 64;                       // box columns (128 bytes)
@@ -119,8 +124,9 @@ constexpr int kColScales = 4 * kTC;             // [rb][col] 1 byte
 constexpr int kColBuf = kColCodes + kColScales; // one tile's staged columnwise results
 constexpr int kQGroups = 2;                     // compute groups per CTA
 constexpr int kQGT = 256;                       // threads per compute group
-// Four compute warpgroups and one control warpgroup, of which one warp
-// works (96 registers per thread: the compute path fits them unspilled).
+// Four compute warpgroups and one warpgroup of two control warps and the
+// two look-ahead warps (96 registers per thread: the compute path fits them
+// unspilled).
 constexpr int kQThreads = kQGroups * kQGT + 128;
 template <bool DUAL>
 __host__ __device__ constexpr int group_bytes() { return 2 * kInStage + (DUAL ? kColBuf : 0); }
@@ -182,6 +188,27 @@ __device__ __forceinline__ void qload_tile(const QuantTileArgs& A, int t, unsign
 #pragma unroll
   for (int j = 0; j < kTC / kBoxC; j++)
     tma_load_2d_hint(dst + j * kBoxBytes, &A.tmap, T.c0 + j * kBoxC, y, b, pol);
+}
+
+// Two columnwise blocks side by side: wc[i] holds row i of the block, low
+// half column j, high half column j + 1.  Each column is regrouped into
+// (row 2k, row 2k + 1) pairs, the layout of a rowwise block, and quantised
+// as one; cj / ck receive the codes of column j / j + 1.  (One rowwise
+// block per column costs fewer instructions than processing the two columns
+// side by side in packed pairs, which needs the pairs transposed for the
+// error chains.)
+template <bool F46>
+__device__ __forceinline__ void quant_col_pair(const uint32_t wc[16], float E, const ScaleEnt* tbl,
+                                               uint32_t cj[2], uint32_t ck[2], uint32_t& sbj,
+                                               uint32_t& sbk) {
+  uint32_t pj[8], pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    pj[i] = __byte_perm(wc[2 * i], wc[2 * i + 1], 0x5410);
+    pk[i] = __byte_perm(wc[2 * i], wc[2 * i + 1], 0x7632);
+  }
+  quant_row_block<F46>(pj, E, tbl, cj[0], cj[1], sbj);
+  quant_row_block<F46>(pk, E, tbl, ck[0], ck[1], sbk);
 }
 
 // ---- compute group k (threads tg = 0 .. 255 of the group)
@@ -333,124 +360,76 @@ __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned cha
   }
 }
 
-// ---- the control warp: copies of the tiles to quantise, and E beside them
+// ---- control warp k: group k's copies, and E beside each
 template <bool F46>
-__device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned char* smem,
-                                              int gbytes, uint64_t* full, uint64_t* empty,
-                                              float* s_E, volatile int* s_least) {
+__device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned char* gbase,
+                                              uint64_t* full, uint64_t* empty, float* s_E,
+                                              volatile int* s_least, int k) {
   const float six_m = F46 ? 1536.0f : 2688.0f;
-  const int lane = threadIdx.x & 31, N = A.ntiles, L = A.la;
+  const int lane = threadIdx.x & 31, N = A.ntiles;
   const int Gq = kQGroups * gridDim.x;
-  const int q0 = kQGroups * (int)blockIdx.x;  // this CTA's first group index
   uint64_t pol = 0;
   if (lane == 0) pol = l2_policy_evict_first();
-  // per group: next iteration to load, next iteration to give E
-  int qi[kQGroups], qe[kQGroups];
-#pragma unroll
-  for (int k = 0; k < kQGroups; k++) qi[k] = qe[k] = 0;
-  // E of the last finished slice; per group, the slice whose word lane 0
-  // is reading and that word
-  int e_s = -1;
+  int e_s = -1;  // the slice whose E is cached
   float e_E = 0.0f;
-  int pf_s[kQGroups];
-  uint32_t pf_w[kQGroups];
-#pragma unroll
-  for (int k = 0; k < kQGroups; k++) {
-    pf_s[k] = -1;
-    pf_w[k] = 0;
-  }
-  uint64_t t_idle = globaltimer_ns();
   bool failed = false;
-  while (true) {
-    bool prog = false;
-    // (1) copies of tiles to quantise, into stages their group has released
-#pragma unroll
-    for (int k = 0; k < kQGroups; k++) {
-      const int g = q0 + k + qi[k] * Gq;
-      if (g < N) {
-        int freed = 1;
-        if (qi[k] >= 2 && lane == 0)
-          freed = mbar_test(&empty[2 * k + (qi[k] & 1)], ((qi[k] - 2) >> 1) & 1);
-        if (__shfl_sync(0xffffffffu, freed, 0)) {
-          if (lane == 0)
-            qload_tile(A, g, smem + k * gbytes + (qi[k] & 1) * kInStage,
-                       &full[2 * k + (qi[k] & 1)], pol);
-          qi[k]++;
-          prog = true;
-        }
-      }
-    }
-    // (2) E beside each loaded tile, once its slice is finished
-#pragma unroll
-    for (int k = 0; k < kQGroups; k++) {
-      if (qe[k] < qi[k]) {
-        const int g = q0 + k + qe[k] * Gq;
-        const int s = (int)A.per_exp.div((uint32_t)g);
-        int have = 0;
-        float E = 0.0f;
-        if (L == 0) {
-          float Gs;
-          global_scales(A.amax[s], six_m, Gs, E);
-          have = 1;
-        } else if (s == e_s) {
-          E = e_E;
-          have = 1;
-        } else {
-          if (lane == 0) {
-            if (pf_s[k] == s && (pf_w[k] & kSliceDone)) {
-              have = 1;
-            } else {
-              pf_w[k] = ld_relaxed_u32(A.ts + s);  // looked at in the next round
-              pf_s[k] = s;
-            }
-          }
-          have = __shfl_sync(0xffffffffu, have, 0);
-          if (have) {
-            const uint32_t w = __shfl_sync(0xffffffffu, pf_w[k], 0);
-            const float Gs = __uint_as_float(w & ~kSliceDone);
-            E = fminf(__frcp_rn(Gs), FLT_MAX);
-            e_s = s;
-            e_E = E;
-          }
-        }
-        if (have) {
-          if (lane == 0) {
-            s_E[2 * k + (qe[k] & 1)] = E;
-            mbar_arrive(&full[2 * k + (qe[k] & 1)]);
-          }
-          qe[k]++;
-          prog = true;
-        }
-      }
-    }
-    // the least tile the groups still need E for bounds the look-ahead
-    int least = N;
-#pragma unroll
-    for (int k = 0; k < kQGroups; k++) least = min(least, q0 + k + qe[k] * Gq);
-    if (lane == 0 && prog) *s_least = least;
-    if (least >= N) break;
-    // lane 0 decides when nothing has moved for too long
-    int stalled = 0;
-    if (lane == 0) {
-      const uint64_t now = globaltimer_ns();
-      if (prog) t_idle = now;
-      else stalled = now - t_idle > kMaxWaitNs;
-    }
-    if (__shfl_sync(0xffffffffu, stalled, 0)) {
+  int j = 0;  // the group's tile count so far
+  for (int g = kQGroups * (int)blockIdx.x + k; g < N; g += Gq, j++) {
+    const int st = j & 1;
+    // the stage holds the group's tile j - 2 until the group releases it
+    int ok = 1;
+    if (j >= 2 && lane == 0) ok = mbar_wait(&empty[2 * k + st], ((j - 2) >> 1) & 1, kWaitTries);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
       failed = true;
+      break;
+    }
+    if (lane == 0) qload_tile(A, g, gbase + st * kInStage, &full[2 * k + st], pol);
+    const int s = (int)A.per_exp.div((uint32_t)g);
+    float E = 0.0f;
+    if (A.la == 0) {
+      float Gs;
+      global_scales(A.amax[s], six_m, Gs, E);
+    } else if (s == e_s) {
+      E = e_E;
+    } else {
+      // the slice's word, once it holds the result (bounded wait)
+      uint32_t w = 0;
+      if (lane == 0) {
+        uint64_t t0 = 0;
+        for (uint32_t i = 0;; i++) {
+          w = ld_relaxed_u32(A.ts + s);
+          if (w & kSliceDone) break;
+          const uint64_t now = globaltimer_ns();
+          if (i == 0) t0 = now;
+          else if (now - t0 > kMaxWaitNs) break;
+          __nanosleep(128);
+        }
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w & kSliceDone) {
+        E = fminf(__frcp_rn(__uint_as_float(w & ~kSliceDone)), FLT_MAX);
+        e_s = s;
+        e_E = E;
+      } else {
+        failed = true;  // the tile still gets its arrival (E = 0) below
+      }
+    }
+    if (lane == 0) {
+      s_E[2 * k + st] = E;
+      mbar_arrive(&full[2 * k + st]);
+      *s_least = g + Gq;  // the next tile this group needs E for
+    }
+    if (failed) {
+      j++;
       break;
     }
   }
   if (failed && lane == 0) {
-    // Nothing moved for too long (a copy never landed or a slice never
-    // finished): report, and give the groups what they wait for so that
-    // they stop on their own.
+    // A stage was never released or a slice never finished: report, and
+    // wait (bounded) for this warp's copies still in flight; the group
+    // stops on its own at its next bounded wait.
     if (A.status) atomicOr(A.status, kStatusTimeout);
-    for (int k = 0; k < kQGroups; k++)
-      for (; qe[k] < qi[k]; qe[k]++) {
-        s_E[2 * k + (qe[k] & 1)] = 0.0f;
-        mbar_arrive(&full[2 * k + (qe[k] & 1)]);
-      }
+    for (int i = max(0, j - 2); i < j; i++) mbar_wait(&full[2 * k + (i & 1)], (i >> 1) & 1, kWaitTries);
   }
 }
 
@@ -466,7 +445,7 @@ __device__ __forceinline__ void quant_lookahead(const QuantTileArgs& A, unsigned
                                                 uint64_t* lafull, uint32_t* s_lamax,
                                                 const volatile int* s_least) {
   const float six_m = F46 ? 1536.0f : 2688.0f;
-  const int lt = threadIdx.x - (kQGroups * kQGT + 32), lane = lt & 31, lw = lt >> 5;
+  const int lt = threadIdx.x - (kQGroups * kQGT + 32 * kQGroups), lane = lt & 31, lw = lt >> 5;
   const int N = A.ntiles, L = A.la;
   const int Gq = kQGroups * gridDim.x;
   const int q0 = kQGroups * (int)blockIdx.x;
@@ -503,7 +482,7 @@ __device__ __forceinline__ void quant_lookahead(const QuantTileArgs& A, unsigned
   auto issue = [&](int n) -> bool {
     const int t = la_tile(n);
     uint64_t t0 = 0;
-    for (uint32_t i = 0; t > *s_least + L; i++) {
+    for (uint32_t i = 0; t > min(s_least[0], s_least[1]) + L; i++) {
       finish_if_last();  // nothing of ours may be held while we wait
       const uint64_t now = globaltimer_ns();
       if (i == 0) t0 = now;
@@ -585,7 +564,7 @@ __global__ void __launch_bounds__(kQThreads, 1) k_quant_tiles(const __grid_const
   uint64_t* const lafull = empty + 2 * kQGroups;                         // [look-ahead stage]
   float* const s_E = reinterpret_cast<float*>(lafull + kS);              // [group][stage]
   uint32_t* const s_lamax = reinterpret_cast<uint32_t*>(s_E + 2 * kQGroups);  // [2][warp]
-  int* const s_least = reinterpret_cast<int*>(s_lamax + 4);
+  int* const s_least = reinterpret_cast<int*>(s_lamax + 4);  // [group]
   const int tid = threadIdx.x;
   const bool misaligned = (smem_u32(smem) & 1023u) != 0;
   if (!misaligned) {
@@ -596,19 +575,20 @@ __global__ void __launch_bounds__(kQThreads, 1) k_quant_tiles(const __grid_const
         mbar_init(&empty[i], 1);  // the group's release
       }
       for (int i = 0; i < kS; i++) mbar_init(&lafull[i], 1);
-      *s_least = kQGroups * (int)blockIdx.x;
+      for (int k = 0; k < kQGroups; k++) s_least[k] = kQGroups * (int)blockIdx.x + k;
       fence_barrier_init();
     }
   } else if (tid == 0 && A.status) {
     atomicOr(A.status, kStatusTimeout);
   }
   __syncthreads();
-  constexpr int kCtl = kQGroups * kQGT;  // the control warp, then the look-ahead warps
-  if (misaligned || tid >= kCtl + 32 + kLaThreads) return;
-  if (tid >= kCtl + 32) {
+  constexpr int kCtl = kQGroups * kQGT;  // the control warps, then the look-ahead warps
+  if (misaligned) return;
+  if (tid >= kCtl + 32 * kQGroups) {
     if (A.la > 0) quant_lookahead<F46, kS>(A, lab, lafull, s_lamax, s_least);
   } else if (tid >= kCtl) {
-    quant_control<F46>(A, smem, kG, full, empty, s_E, s_least);
+    const int k = (tid - kCtl) >> 5;
+    quant_control<F46>(A, smem + k * kG, full, empty, s_E, s_least + k, k);
   } else {
     quant_group<F46, DUAL>(A, smem + (tid / kQGT) * kG, tbl, full, empty, s_E, tid / kQGT,
                            tid % kQGT);
