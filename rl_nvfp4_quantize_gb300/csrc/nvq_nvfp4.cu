@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(kActStreamThreads, 1)
     k_act_stream(const uint16_t* __restrict__ x, int64_t T, int H, uint8_t* __restrict__ codes,
                  uint8_t* __restrict__ scales, float* __restrict__ token_scale,
                  int* __restrict__ status, int tiled) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int S = act_stream_stages(H);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rowbytes = 2u * (uint32_t)H;

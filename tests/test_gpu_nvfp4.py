@@ -311,11 +311,13 @@ def test_transposed_dequant_ragged_tiles(nvq, oracle_mod, shape):
     assert_same(u16(dt), oracle_mod.nvfp4_dequant_t(codes, scales, G, R, K), "dequant_t")
 
 
-@pytest.mark.parametrize("T,H", [(8000, 2064), (2500, 6400), (4097, 6144), (300, 2080)])
+@pytest.mark.parametrize("T,H", [(8000, 2064), (2500, 6400), (4097, 6144), (300, 2080),
+                                 (257, 3216)])
 def test_act_streamed_rows_wrap_the_ring(nvq, oracle_mod, T, H):
     """Rows of 2048 < H <= 6400 values stream through each warp's ring of
     row buffers; with more rows per warp than buffers the ring wraps (its
-    barriers change phase): same bytes as the oracle."""
+    barriers change phase); 6144, 6400 and 3216 leave one buffer per warp,
+    2064 and 2080 several: same bytes as the oracle."""
     from rl_nvfp4_quantize_gb300 import synth
     x = synth.activations(T, H, seed=T + H)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")

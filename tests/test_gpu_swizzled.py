@@ -59,7 +59,7 @@ def test_dual_swizzled_scales(nvq, oracle_mod, E, R, K):
     assert np.array_equal(_np(sc), oracle_mod.scales_tiled(ocol["scales"]))
 
 
-@pytest.mark.parametrize("T,H", [(256, 512), (37, 208)])
+@pytest.mark.parametrize("T,H", [(256, 512), (37, 208), (300, 6144), (129, 3216)])
 def test_act_swizzled_scales(nvq, oracle_mod, T, H):
     from rl_nvfp4_quantize_gb300 import synth
     x = synth.activations(T, H, seed=T + H, device="cuda")
