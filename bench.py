@@ -484,6 +484,9 @@ def main():
         dram = load_traffic(n)
         if dram:
             e["dram_over_algorithmic"] = round(dram / b, 3)
+        sec = load_sectors(n)
+        if sec:
+            e["sectors"] = sec
         breakdown[n] = e
     st = int(wl.status.item())
     n_routed = int(wl.nhit.item())  # of the timed steps' router (the context reuses the buffer)
@@ -561,11 +564,7 @@ def issue_view(kernel_name, ms, shape):
     """The dominant call seen as instruction-issue bound: executed thread
     instructions per second (instructions per element from the committed ncu
     capture x elements per second measured here) against ISSUE_PEAK."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    try:
-        ipe = json.load(open(p)).get("_instr_per_elem", {}).get(kernel_name)
-    except (OSError, ValueError):
-        ipe = None
+    ipe = load_profile_table().get("_instr_per_elem", {}).get(kernel_name)
     if not ipe:
         return None
     n = shape[0] * shape[1] * shape[2]
@@ -575,18 +574,30 @@ def issue_view(kernel_name, ms, shape):
             "frac": round(achieved / ISSUE_PEAK, 4)}
 
 
-def load_traffic(kernel_name):
-    """DRAM bytes per call of the dominant entry point from the committed ncu
-    summary, if one was taken of the current kernels."""
+def load_profile_table():
+    """The committed per-call ncu figures (profiles/traffic.json), or {}."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
-        return None
     try:
         d = json.load(open(p))
-        v = d.get(kernel_name)
-        return v if isinstance(v, (int, float)) else None
+        return d if isinstance(d, dict) else {}
     except (OSError, ValueError):
+        return {}
+
+
+def load_traffic(kernel_name):
+    """DRAM bytes per call of an entry point from the committed ncu capture of
+    the current kernels on the full-size workload; None for any other size."""
+    if GATE_UP[0] != 256:
         return None
+    v = load_profile_table().get(kernel_name)
+    return v if isinstance(v, (int, float)) else None
+
+
+def load_sectors(kernel_name):
+    """Sector efficiency of a call's global loads and stores (useful bytes per
+    32-byte sector moved between L1 and L2) from the committed ncu capture."""
+    v = load_profile_table().get("_sectors", {}).get(kernel_name)
+    return v if isinstance(v, dict) else None
 
 
 def cuda_timed(fn, reps):
