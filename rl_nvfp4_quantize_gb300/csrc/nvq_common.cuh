@@ -303,19 +303,13 @@ __device__ __forceinline__ float row_candidate(const float2 t2[8], const ScaleEn
   return __fadd_rn(acc.x, acc.y);
 }
 
-// Quantises one rowwise block given its 8 bf16x2 words, the block amax (FP32)
-// and the slice's encode factor E.  Outputs the two code words and the scale
-// byte.
+// Quantises one block given its scaled values t2[k] = (t_2k, t_2k+1) (t = x E)
+// and its scaled amax a = fl(bamax E).  Outputs the two code words and the
+// scale byte.
 template <bool F46>
-__device__ __forceinline__ void quant_row_block_amax(const uint32_t w[8], float bamax, float E,
-                                                     const ScaleEnt* tbl, uint32_t& c0,
-                                                     uint32_t& c1, uint32_t& sb) {
-  const float a = __fmul_rn(bamax, E);
+__device__ __forceinline__ void quant_block_t2(const float2 t2[8], float a, const ScaleEnt* tbl,
+                                               uint32_t& c0, uint32_t& c1, uint32_t& sb) {
   const uint32_t sbytes = block_scale_bytes(a);
-  float2 t2[8];
-  const float2 E2 = make_float2(E, E);
-#pragma unroll
-  for (int k = 0; k < 8; k++) t2[k] = __fmul2_rn(widen2(w[k]), E2);
   const uint32_t s6 = sbytes & 0x7fu;
   const float e6 = row_candidate(t2, tbl[s6], c0, c1);
   sb = s6;
@@ -329,6 +323,20 @@ __device__ __forceinline__ void quant_row_block_amax(const uint32_t w[8], float 
       sb = s4;
     }
   }
+}
+
+// Quantises one rowwise block given its 8 bf16x2 words, the block amax (FP32)
+// and the slice's encode factor E.  Outputs the two code words and the scale
+// byte.
+template <bool F46>
+__device__ __forceinline__ void quant_row_block_amax(const uint32_t w[8], float bamax, float E,
+                                                     const ScaleEnt* tbl, uint32_t& c0,
+                                                     uint32_t& c1, uint32_t& sb) {
+  float2 t2[8];
+  const float2 E2 = make_float2(E, E);
+#pragma unroll
+  for (int k = 0; k < 8; k++) t2[k] = __fmul2_rn(widen2(w[k]), E2);
+  quant_block_t2<F46>(t2, __fmul_rn(bamax, E), tbl, c0, c1, sb);
 }
 
 template <bool F46>

@@ -191,24 +191,31 @@ __device__ __forceinline__ void qload_tile(const QuantTileArgs& A, int t, unsign
 }
 
 // Two columnwise blocks side by side: wc[i] holds row i of the block, low
-// half column j, high half column j + 1.  Each column is regrouped into
-// (row 2k, row 2k + 1) pairs, the layout of a rowwise block, and quantised
-// as one; cj / ck receive the codes of column j / j + 1.  (One rowwise
-// block per column costs fewer instructions than processing the two columns
-// side by side in packed pairs, which needs the pairs transposed for the
-// error chains.)
+// half column j, high half column j + 1.  One magnitude-max tree over the 16
+// words gives both column maxima; each value is widened and scaled into the
+// pair layout of a rowwise block, (row 2k, row 2k + 1), and each column is
+// quantised as one rowwise block; cj / ck receive the codes of column j /
+// j + 1.  (The pairs come straight from the widening, so no byte regroup is
+// needed; processing the two columns side by side in packed pairs instead
+// would need the pairs transposed for the error chains.)
 template <bool F46>
 __device__ __forceinline__ void quant_col_pair(const uint32_t wc[16], float E, const ScaleEnt* tbl,
                                                uint32_t cj[2], uint32_t ck[2], uint32_t& sbj,
                                                uint32_t& sbk) {
-  uint32_t pj[8], pk[8];
+  uint32_t m = maxabs2(wc[0], wc[1]);
 #pragma unroll
-  for (int i = 0; i < 8; i++) {
-    pj[i] = __byte_perm(wc[2 * i], wc[2 * i + 1], 0x5410);
-    pk[i] = __byte_perm(wc[2 * i], wc[2 * i + 1], 0x7632);
+  for (int i = 2; i < 16; i++) m = maxabs2(m, wc[i]);
+  m &= 0x7fff7fffu;
+  const float2 E2 = make_float2(E, E);
+  float2 tj[8], tk[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    const float2 r0 = widen2(wc[2 * k]), r1 = widen2(wc[2 * k + 1]);
+    tj[k] = __fmul2_rn(make_float2(r0.x, r1.x), E2);
+    tk[k] = __fmul2_rn(make_float2(r0.y, r1.y), E2);
   }
-  quant_row_block<F46>(pj, E, tbl, cj[0], cj[1], sbj);
-  quant_row_block<F46>(pk, E, tbl, ck[0], ck[1], sbk);
+  quant_block_t2<F46>(tj, __fmul_rn(lo_f(m), E), tbl, cj[0], cj[1], sbj);
+  quant_block_t2<F46>(tk, __fmul_rn(hi_f(m), E), tbl, ck[0], ck[1], sbk);
 }
 
 // ---- compute group k (threads tg = 0 .. 255 of the group)
