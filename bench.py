@@ -698,7 +698,7 @@ def measure_context(wl, dev, peak):
 
 
 def measure_nest(wl, peak):
-    """The nested (double-quantised) NF4 absmax (row F4) of the whole gate_up
+    """The nested (double-quantised) NF4 absmax of the whole gate_up
     stack's absmax, [256, 4096 x 6144 / 64] FP32: nf4_absmax_nest (4 B in;
     1 B code + 4/256 B block maximum out per value) and nf4_absmax_unnest
     (the reverse)."""
@@ -723,7 +723,7 @@ def measure_nest(wl, peak):
 
 
 def measure_mxfp8(wl, peak):
-    """MXFP8 (row F4) of the 32-expert gate_up stack [32, 4096, 6144]:
+    """MXFP8 of the 32-expert gate_up stack [32, 4096, 6144]:
     rowwise only (bf16 in 2 B, codes 1 B + scales 1/32 B per element) and
     rowwise + columnwise from one read (2 + 2 x (1 + 1/32) B per element), and
     the dequantisation of the rowwise copy (1 + 1/32 B in, 2 B out)."""

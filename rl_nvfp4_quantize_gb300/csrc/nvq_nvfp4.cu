@@ -77,7 +77,7 @@ cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q) {
 //     It spends its time blocked in barrier waits, not polling, so the
 //     compute warps keep the issue slots.
 //   * the look-ahead stream computes the slice amax in the same pass over
-//     the stack (S1): it streams this CTA's look-ahead tiles (the same tile
+//     the stack: it streams this CTA's look-ahead tiles (the same tile
 //     indices as its two groups, up to L tiles ahead of them) through a
 //     small ring, reduces each to its magnitude maximum, and keeps the
 //     per-slice results described below.
@@ -111,7 +111,7 @@ cudaError_t launch_zero_f32(float* p, int64_t n, cudaStream_t s, float* q) {
 //   rowwise pass   : 1024 blocks of 1x16, four per thread, results stored
 //                    straight to global (8 code bytes + 1 scale byte);
 //   columnwise pass: 256 units of 16 rows x 4 columns, one per thread, each
-//                    column regrouped into the pair layout of a rowwise block
+//                    column widened into the pair layout of a rowwise block
 //                    and quantised as one; the results are staged and written
 //                    as contiguous runs of the transposed [in, out/2] layout.
 // Inside a swizzled box, 16-byte chunk c of row r sits at chunk c ^ (r & 7).
