@@ -599,7 +599,7 @@ ORACLE_API void oracle_f32_to_bf16_n(const float* x, uint16_t* out, int64_t n)
 }
 
 /* ------------------------------------------------------------------------ */
-/* MXFP8: the format "The 4-bitter Lesson" ("Key claims") used to         */
+/* MXFP8: the format "The 4-bitter Lesson" ("Key claims") used to            */
 /* validate the dequantised backward before NVFP4.  The pages name it only;  */
 /* its definition is the OCP Microscaling (MX) one: blocks of 32 consecutive */
 /* elements share one E8M0 scale X = 2^s, and each element is stored as the  */
