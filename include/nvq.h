@@ -453,9 +453,9 @@ NVQ_API int nvq_debug_count_timeout(uint32_t max_polls, const uint32_t* counter,
 /*
  * nvq_debug_set_quant_lead -- how far beyond one slice the single-pass amax
  * of nvfp4_quantize and nvfp4_quantize_dual reads ahead of the tiles being
- * quantised, in waves of the kernel's grid (default 2, also the least that
- * keeps every wait of the kernel acyclic).  Outputs do not depend on it;
- * at 2 the slices' amax complete shortly before they are needed.
+ * quantised, in waves of the kernel's grid (default 2; the kernel's waits
+ * stay acyclic for any lead of one wave or more).  Outputs do not depend on
+ * it; at 2 the slices' amax complete shortly before they are needed.
  * Process-wide setting for tests and tuning, read at each call.
  *   waves   2 .. 8 (other values return NVQ_ERR_SHAPE and change nothing)
  * Host only; returns NVQ_OK.

@@ -401,17 +401,7 @@ __device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned c
     } else {
       // the slice's word, once it holds the result (bounded wait)
       uint32_t w = 0;
-      if (lane == 0) {
-        uint64_t t0 = 0;
-        for (uint32_t i = 0;; i++) {
-          w = ld_relaxed_u32(A.ts + s);
-          if (w & kSliceDone) break;
-          const uint64_t now = globaltimer_ns();
-          if (i == 0) t0 = now;
-          else if (now - t0 > kMaxWaitNs) break;
-          __nanosleep(128);
-        }
-      }
+      if (lane == 0) wait_done(A.ts + s, w);
       w = __shfl_sync(0xffffffffu, w, 0);
       if (w & kSliceDone) {
         E = fminf(__frcp_rn(__uint_as_float(w & ~kSliceDone)), FLT_MAX);
