@@ -235,6 +235,7 @@ __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned cha
   const int cb = tg & 15;
   const int rb0 = 2 * warp + (((tg >> 4) ^ (tg >> 2)) & 1);
   const int rbox = (cb >> 2) * kBoxBytes, rchunk = 2 * (cb & 3);
+  const int row_lo = (rchunk ^ (rb0 & 7)) << 4, row_hi = ((rchunk + 1) ^ (rb0 & 7)) << 4;
   // columnwise geometry: row block cr, columns 4q .. 4q+3
   const int cr = warp >> 1, q = ((warp & 1) << 5) + lane;
   const int cbox = (q >> 4) * kBoxBytes, cchunk = (q & 15) >> 1, chalf = (q & 1) * 8;
@@ -313,29 +314,32 @@ __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned cha
     const unsigned char* tile = gbase + st * kInStage;
     const QTile T = qtile_of(A, g);
 
-    // rowwise blocks: four per thread, 16 rows apart
+    // rowwise blocks: four per thread, 16 rows apart (rows r = rb0 + 16 kk
+    // share r & 7, so the swizzled chunk offsets are fixed per thread and the
+    // pointers step by a constant)
     {
       const int64_t grow0 = (int64_t)T.e * rows + T.r0 + rb0;
       uint8_t* pc = A.codes_row + grow0 * cols_h + (T.c0 >> 1) + cb * 8;
       uint8_t* ps = A.scales_row + grow0 * cols_16 + (T.c0 >> 4) + cb;
-      const bool cvalid = cb * 16 < T.cv;
+      const unsigned char* rowp = tile + rbox + rb0 * 128;
+      const int nkk = cb * 16 < T.cv ? min(4, (T.rv - rb0 + 15) >> 4) : 0;
 #pragma unroll 1
-      for (int kk = 0; kk < 4; kk++) {
-        const int r = rb0 + 16 * kk;
-        if (cvalid && r < T.rv) {
-          const unsigned char* rowp = tile + rbox + r * 128;
-          const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((rchunk ^ (r & 7)) << 4));
-          const uint4 hi = *reinterpret_cast<const uint4*>(rowp + (((rchunk + 1) ^ (r & 7)) << 4));
-          const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          uint32_t c0w, c1w, sb;
-          quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
-          stg_stream_v2(pc + 16 * kk * cols_h, c0w, c1w);
-          if (A.tiled)
-            A.scales_row[T.e * A.sl_row +
-                         scale_off_tiled(T.r0 + r, (T.c0 >> 4) + cb, A.ct_row)] = (uint8_t)sb;
-          else
-            stg_stream_u8(ps + 16 * kk * cols_16, sb);
-        }
+      for (int kk = 0; kk < nkk; kk++) {
+        const uint4 lo = *reinterpret_cast<const uint4*>(rowp + row_lo);
+        const uint4 hi = *reinterpret_cast<const uint4*>(rowp + row_hi);
+        const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        uint32_t c0w, c1w, sb;
+        quant_row_block<F46>(wv, E, tbl, c0w, c1w, sb);
+        stg_stream_v2(pc, c0w, c1w);
+        if (A.tiled)
+          A.scales_row[T.e * A.sl_row +
+                       scale_off_tiled(T.r0 + rb0 + 16 * kk, (T.c0 >> 4) + cb, A.ct_row)] =
+              (uint8_t)sb;
+        else
+          stg_stream_u8(ps, sb);
+        rowp += 16 * 128;
+        pc += 16 * cols_h;
+        ps += 16 * cols_16;
       }
     }
 
@@ -503,11 +507,19 @@ __device__ __forceinline__ void quant_lookahead(const QuantTileArgs& A, unsigned
                                            kTR);
       // thread lt reads 16-byte chunks lt + 64 i: row (lt >> 3) + 8 (i & 7) of its box
       const unsigned char* p = lab + st * kInStage + lt * 16;
+      if (rv == kTR) {
 #pragma unroll 8
-      for (int i = 0; i < kInStage / (16 * kLaThreads); i++) {
-        if ((lt >> 3) + 8 * (i & 7) < rv) {
+        for (int i = 0; i < kInStage / (16 * kLaThreads); i++) {
           const uint4 v = *reinterpret_cast<const uint4*>(p + i * 16 * kLaThreads);
           m[i & 3] = maxabs2_nan(m[i & 3], maxabs2_nan(maxabs2_nan(v.x, v.y), maxabs2_nan(v.z, v.w)));
+        }
+      } else {
+#pragma unroll 8
+        for (int i = 0; i < kInStage / (16 * kLaThreads); i++) {
+          if ((lt >> 3) + 8 * (i & 7) < rv) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p + i * 16 * kLaThreads);
+            m[i & 3] = maxabs2_nan(m[i & 3], maxabs2_nan(maxabs2_nan(v.x, v.y), maxabs2_nan(v.z, v.w)));
+          }
         }
       }
     }
