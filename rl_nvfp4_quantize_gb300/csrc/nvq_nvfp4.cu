@@ -248,14 +248,29 @@ __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned cha
   // [rb][col] 8 bytes, the two halves of each 32-byte group swapped as
   // above, then scales [rb][col] 1 byte), leave as contiguous runs of the
   // transposed layout: thread c writes column c.
+  // write-out constants of this thread's column c = tg: its staged code
+  // offset, and whether whole tiles take the one-store paths (rows a
+  // multiple of 64, 32-byte aligned columnwise codes, linear scales)
+  const int soff = (tg >> 2) * 32 + ((((tg >> 1) & 1) ^ ((tg >> 4) & 1)) << 4) + (tg & 1) * 8;
+  const bool col_fast = (rows & 63) == 0 && A.col32 && !A.tiled;
   auto write_col = [&](const QTile& T) {
     const int c = tg;
-    if (c < T.cv) {
+    if (col_fast && T.rv == kTR && c < T.cv) {
+      const int64_t grow = (int64_t)T.e * cols + T.c0 + c;
+      const uint2 v0 = *reinterpret_cast<const uint2*>(colc + soff);
+      const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + soff);
+      const uint2 v2 = *reinterpret_cast<const uint2*>(colc + 2 * kTC * 8 + soff);
+      const uint2 v3 = *reinterpret_cast<const uint2*>(colc + 3 * kTC * 8 + soff);
+      const uint32_t v8[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+      stg256_stream(A.codes_col + grow * rows_h + (T.r0 >> 1), v8);
+      const uint32_t b01 = __byte_perm(cols_s[c], cols_s[kTC + c], 0x0040);
+      const uint32_t b23 = __byte_perm(cols_s[2 * kTC + c], cols_s[3 * kTC + c], 0x0040);
+      stg_stream_u32(A.scales_col + grow * rows_16 + (T.r0 >> 4), __byte_perm(b01, b23, 0x5410));
+    } else if (c < T.cv) {
       const int nrb = T.rv >> 4;
       const int64_t grow = (int64_t)T.e * cols + T.c0 + c;
       uint8_t* dstc = A.codes_col + grow * rows_h + (T.r0 >> 1);
       uint8_t* dsts = A.scales_col + grow * rows_16 + (T.r0 >> 4);
-      const int soff = (c >> 2) * 32 + ((((c >> 1) & 1) ^ ((c >> 4) & 1)) << 4) + (c & 1) * 8;
       if (nrb == 4 && (rows & 31) == 0) {
         const uint2 v0 = *reinterpret_cast<const uint2*>(colc + soff);
         const uint2 v1 = *reinterpret_cast<const uint2*>(colc + kTC * 8 + soff);
