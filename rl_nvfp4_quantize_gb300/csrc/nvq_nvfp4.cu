@@ -517,9 +517,12 @@ __device__ __forceinline__ void quant_lookahead(const QuantTileArgs& A, unsigned
     bool landed = __shfl_sync(0xffffffffu, (int)ok, 0) && mbar_wait(&lafull[st], (n / S) & 1, kWaitTries);
     uint32_t m[4] = {0, 0, 0, 0};
     if (landed) {
-      const int rv = min(kTR, A.rows - (int)A.by_tiles_c.div((uint32_t)la_tile(n) -
-                                                             A.per_exp.div((uint32_t)la_tile(n)) * P) *
-                                           kTR);
+      const int rv = (A.rows & (kTR - 1)) == 0
+                         ? kTR
+                         : min(kTR, A.rows - (int)A.by_tiles_c.div(
+                                                 (uint32_t)la_tile(n) -
+                                                 A.per_exp.div((uint32_t)la_tile(n)) * P) *
+                                                 kTR);
       // thread lt reads 16-byte chunks lt + 64 i: row (lt >> 3) + 8 (i & 7) of its box
       const unsigned char* p = lab + st * kInStage + lt * 16;
       if (rv == kTR) {
