@@ -503,7 +503,7 @@ __device__ __forceinline__ void quant_lookahead(const QuantTileArgs& A, unsigned
       const uint64_t now = globaltimer_ns();
       if (i == 0) t0 = now;
       else if (now - t0 > kMaxWaitNs) return false;
-      __nanosleep(256);
+      __nanosleep(64);
     }
     qload_tile(A, t, lab + (n % S) * kInStage, &lafull[n % S], pol);
     return true;
