@@ -180,14 +180,31 @@ __device__ __forceinline__ QTile qtile_of(const QuantTileArgs& A, int t) {
 
 // Thread `lane 0` of the control warp: the four box loads of tile t into
 // `dst`, completing on `b` (parts out of range are zero-filled).
-__device__ __forceinline__ void qload_tile(const QuantTileArgs& A, int t, unsigned char* dst,
-                                           uint64_t* b, uint64_t pol) {
-  const QTile T = qtile_of(A, t);
+__device__ __forceinline__ void qload_tile(const QuantTileArgs& A, const QTile& T,
+                                           unsigned char* dst, uint64_t* b, uint64_t pol) {
   mbar_arrive_expect_tx(b, kInStage);
   const int y = (int)(T.e * (uint32_t)A.rows) + T.r0;
 #pragma unroll
   for (int j = 0; j < kTC / kBoxC; j++)
     tma_load_2d_hint(dst + j * kBoxBytes, &A.tmap, T.c0 + j * kBoxC, y, b, pol);
+}
+__device__ __forceinline__ void qload_tile(const QuantTileArgs& A, int t, unsigned char* dst,
+                                           uint64_t* b, uint64_t pol) {
+  qload_tile(A, qtile_of(A, t), dst, b, pol);
+}
+
+// A tile's place, as the control warp hands it to the group beside E.
+__device__ __forceinline__ uint4 qtile_pack(const QTile& T) {
+  return make_uint4(T.e, (uint32_t)T.r0, (uint32_t)T.c0, ((uint32_t)T.rv << 16) | (uint32_t)T.cv);
+}
+__device__ __forceinline__ QTile qtile_unpack(const uint4 p) {
+  QTile T;
+  T.e = p.x;
+  T.r0 = (int)p.y;
+  T.c0 = (int)p.z;
+  T.rv = (int)(p.w >> 16);
+  T.cv = (int)(p.w & 0xffffu);
+  return T;
 }
 
 // Two columnwise blocks side by side: wc[i] holds row i of the block, low
@@ -222,7 +239,7 @@ __device__ __forceinline__ void quant_col_pair(const uint32_t wc[16], float E, c
 template <bool F46, bool DUAL>
 __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned char* gbase,
                                             const ScaleEnt* tbl, uint64_t* full, uint64_t* empty,
-                                            const float* s_E, int k, int tg) {
+                                            const float* s_E, const uint4* s_T, int k, int tg) {
   const int rows = A.rows, cols = A.cols, N = A.ntiles;
   const int Gq = kQGroups * gridDim.x;
   const int64_t cols_h = cols >> 1, cols_16 = cols >> 4, rows_h = rows >> 1, rows_16 = rows >> 4;
@@ -327,7 +344,7 @@ __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned cha
     }
     const float E = s_E[2 * k + st];
     const unsigned char* tile = gbase + st * kInStage;
-    const QTile T = qtile_of(A, g);
+    const QTile T = qtile_unpack(s_T[2 * k + st]);
 
     // rowwise blocks: four per thread, 16 rows apart (rows r = rb0 + 16 kk
     // share r & 7, so the swizzled chunk offsets are fixed per thread and the
@@ -389,7 +406,7 @@ __device__ __forceinline__ void quant_group(const QuantTileArgs& A, unsigned cha
 // ---- control warp k: group k's copies, and E beside each
 template <bool F46>
 __device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned char* gbase,
-                                              uint64_t* full, uint64_t* empty, float* s_E,
+                                              uint64_t* full, uint64_t* empty, float* s_E, uint4* s_T,
                                               volatile int* s_least, int k) {
   const float six_m = F46 ? 1536.0f : 2688.0f;
   const int lane = threadIdx.x & 31, N = A.ntiles;
@@ -409,7 +426,8 @@ __device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned c
       failed = true;
       break;
     }
-    if (lane == 0) qload_tile(A, g, gbase + st * kInStage, &full[2 * k + st], pol);
+    const QTile T = qtile_of(A, g);
+    if (lane == 0) qload_tile(A, T, gbase + st * kInStage, &full[2 * k + st], pol);
     const int s = (int)A.per_exp.div((uint32_t)g);
     float E = 0.0f;
     if (A.la == 0) {
@@ -432,6 +450,7 @@ __device__ __forceinline__ void quant_control(const QuantTileArgs& A, unsigned c
     }
     if (lane == 0) {
       s_E[2 * k + st] = E;
+      s_T[2 * k + st] = qtile_pack(T);
       mbar_arrive(&full[2 * k + st]);
       *s_least = g + Gq;  // the next tile this group needs E for
     }
@@ -585,8 +604,9 @@ __global__ void __launch_bounds__(kQThreads, 1) k_quant_tiles(const __grid_const
   constexpr int kS = la_stages<DUAL>();
   unsigned char* const lab = smem + kQGroups * kG;
   ScaleEnt* const tbl = reinterpret_cast<ScaleEnt*>(lab + kS * kInStage);
-  uint64_t* const full = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(tbl) +
-                                                     kScaleTableBytes);  // [group][stage]
+  uint4* const s_T = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(tbl) +
+                                               kScaleTableBytes);          // [group][stage]
+  uint64_t* const full = reinterpret_cast<uint64_t*>(s_T + 2 * kQGroups);  // [group][stage]
   uint64_t* const empty = full + 2 * kQGroups;                           // [group][stage]
   uint64_t* const lafull = empty + 2 * kQGroups;                         // [look-ahead stage]
   float* const s_E = reinterpret_cast<float*>(lafull + kS);              // [group][stage]
@@ -615,9 +635,9 @@ __global__ void __launch_bounds__(kQThreads, 1) k_quant_tiles(const __grid_const
     if (A.la > 0) quant_lookahead<F46, kS>(A, lab, lafull, s_lamax, s_least);
   } else if (tid >= kCtl) {
     const int k = (tid - kCtl) >> 5;
-    quant_control<F46>(A, smem + k * kG, full, empty, s_E, s_least + k, k);
+    quant_control<F46>(A, smem + k * kG, full, empty, s_E, s_T, s_least + k, k);
   } else {
-    quant_group<F46, DUAL>(A, smem + (tid / kQGT) * kG, tbl, full, empty, s_E, tid / kQGT,
+    quant_group<F46, DUAL>(A, smem + (tid / kQGT) * kG, tbl, full, empty, s_E, s_T, tid / kQGT,
                            tid % kQGT);
   }
 }
