@@ -151,12 +151,15 @@ NVQ_API const char* nvq_status_string(int code);
  *   status   out  device int, nullable (with NVQ_AMAX_GIVEN the input is not
  *            scanned, so only a non-finite given amax is reported)
  *
- * The stack is read from HBM once: the kernel reduces each slice's amax
- * from tiles it loads a little more than one slice ahead of the tiles it
- * quantises, which are then read again from L2.  The quantising kernel is
- * a cooperative launch (all its CTAs resident at once), because a CTA that
- * starts a slice waits, bounded, for the amax of that slice; if a wait
- * gives up, NVQ_STATUS_TIMEOUT is set in *status and the outputs are
+ * One pass over the stack: the kernel reduces each slice's amax from tiles
+ * it loads a little more than one slice ahead of the tiles it quantises,
+ * and reads those tiles again to quantise them.  The second read hits L2
+ * while that window (one slice plus two waves of tiles, and the outputs
+ * written meanwhile) fits in it, as for [256, 6144, 2048] slices; slices as
+ * large as 4096 x 6144 go back to HBM for most of it.  The quantising
+ * kernel is a cooperative launch (all its CTAs resident at once), because a
+ * CTA that starts a slice waits, bounded, for the amax of that slice; if a
+ * wait gives up, NVQ_STATUS_TIMEOUT is set in *status and the outputs are
  * unspecified.
  */
 NVQ_API int nvfp4_quantize(const uint16_t* w, int64_t nexp, int64_t rows, int64_t cols,
