@@ -86,15 +86,30 @@ __global__ void __launch_bounds__(kNqThreads)
   const unsigned char* const lane_tbl = smem + (threadIdx.x & 31) * 8;
   const int64_t stride = (int64_t)gridDim.x * kNqThreads;
   const float2 k16 = make_float2(16.0f, 16.0f), k96 = make_float2(96.0f, 96.0f);
+  const bool w32 = (reinterpret_cast<uintptr_t>(w) & 31) == 0;
   // The loop bound is taken at the warp's first lane so that whole warps
   // stay together for the shuffle; lanes past the end only skip the stores.
   for (int64_t h = (int64_t)blockIdx.x * kNqThreads + threadIdx.x; h - (threadIdx.x & 31) < nhalf;
        h += stride) {
     const bool act = h < nhalf;
+    // the half block's 64 bytes as two 32-byte loads (one full sector each)
+    // when the stack is 32-byte aligned, else as four 16-byte loads
     uint4 v[4];
+    if (act && !w32) {
 #pragma unroll
-    for (int u = 0; u < 4; u++)
-      v[u] = act ? __ldg(reinterpret_cast<const uint4*>(w + h * 32 + u * 8)) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 4; u++) v[u] = __ldg(reinterpret_cast<const uint4*>(w + h * 32 + u * 8));
+    } else if (act) {
+      uint32_t a[8], b[8];
+      ldg32(w + h * 32, a);
+      ldg32(w + h * 32 + 16, b);
+      v[0] = make_uint4(a[0], a[1], a[2], a[3]);
+      v[1] = make_uint4(a[4], a[5], a[6], a[7]);
+      v[2] = make_uint4(b[0], b[1], b[2], b[3]);
+      v[3] = make_uint4(b[4], b[5], b[6], b[7]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; u++) v[u] = make_uint4(0, 0, 0, 0);
+    }
     uint32_t m = maxabs2_nan(v[0].x, v[0].y);
     m = maxabs2_nan(m, v[0].z);
     m = maxabs2_nan(m, v[0].w);

@@ -32,6 +32,22 @@ def test_nf4_quantize_dequant_parity(nvq, oracle_mod, shape):
     assert_same(u16(d), oracle_mod.nf4_dequant(o["codes"], o["absmax"], E, R, K), "dequant")
 
 
+def test_nf4_stack_16_byte_aligned(nvq, oracle_mod):
+    """A stack that is 16- but not 32-byte aligned takes the 16-byte loads
+    instead of the 32-byte ones: same bytes as the oracle."""
+    from rl_nvfp4_quantize_gb300 import synth
+    E, R, K = 2, 48, 320
+    w = synth.expert_weights(E, R, K, seed=91)
+    buf = torch.empty(w.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    wv = buf[8:].view(E, R, K)
+    wv.copy_(w.cuda())
+    assert wv.data_ptr() % 32 == 16
+    r = nvq.nf4_quantize(wv)
+    o = oracle_mod.nf4_quantize(u16(w))
+    assert_same(f32(r["absmax"]).view(np.uint32), o["absmax"].view(np.uint32), "absmax")
+    assert_same(u8(r["codes"]), o["codes"], "codes")
+
+
 def test_nf4_every_bf16_value(nvq, oracle_mod):
     """All finite bf16 patterns, in blocks whose maximum is 1.0 and 300.0."""
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
