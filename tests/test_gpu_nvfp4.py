@@ -311,6 +311,24 @@ def test_transposed_dequant_ragged_tiles(nvq, oracle_mod, shape):
     assert_same(u16(dt), oracle_mod.nvfp4_dequant_t(codes, scales, G, R, K), "dequant_t")
 
 
+@pytest.mark.parametrize("H", [2048, 208])
+def test_act_rows_16_byte_aligned(nvq, oracle_mod, H):
+    """Activations 16- but not 32-byte aligned (the loads are 16-byte ones):
+    same bytes as the oracle."""
+    from rl_nvfp4_quantize_gb300 import synth
+    T = 37
+    x = synth.activations(T, H, seed=H + 5)
+    buf = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    xv = buf[8:].view(T, H)
+    xv.copy_(x.cuda())
+    assert xv.data_ptr() % 32 == 16
+    r = nvq.act_quantize_per_token(xv, four_over_six=True)
+    o = oracle_mod.act_quantize_per_token(u16(x), four_over_six=True)
+    assert_same(u8(r["codes"]), o["codes"], "codes")
+    assert_same(u8(r["scales"]), o["scales"], "scales")
+    assert_same(f32(r["token_scale"]).view(np.uint32), o["token_scale"].view(np.uint32), "token_scale")
+
+
 @pytest.mark.parametrize("T,H", [(8000, 2064), (2500, 6400), (4097, 6144), (300, 2080),
                                  (257, 3216)])
 def test_act_streamed_rows_wrap_the_ring(nvq, oracle_mod, T, H):
