@@ -46,14 +46,6 @@ __device__ __forceinline__ uint32_t maxabs2_nan(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Per half: unsigned 16-bit max of the magnitude bits.  NaN patterns compare
-// above infinity, so a NaN anywhere propagates to the result.
-__device__ __forceinline__ uint32_t umaxmag2(uint32_t m, uint32_t w) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(m), "r"(w & 0x7fff7fffu));
-  return d;
-}
-
 // The larger of the two magnitudes of a max-abs word, as FP32.
 __device__ __forceinline__ float amax_of(uint32_t m) {
   m &= 0x7fff7fffu;

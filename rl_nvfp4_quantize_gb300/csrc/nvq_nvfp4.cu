@@ -795,19 +795,20 @@ __global__ void __launch_bounds__(kActThreads)
         const uint4 hi = ldg_stream(xr + b * 16 + 8);
         wr[k][0] = lo.x; wr[k][1] = lo.y; wr[k][2] = lo.z; wr[k][3] = lo.w;
         wr[k][4] = hi.x; wr[k][5] = hi.y; wr[k][6] = hi.z; wr[k][7] = hi.w;
-        uint32_t mk = 0;
+        uint32_t mk = maxabs2_nan(wr[k][0], wr[k][1]);
 #pragma unroll
-        for (int i = 0; i < 8; i++) mk = umaxmag2(mk, wr[k][i]);
+        for (int i = 2; i < 8; i++) mk = maxabs2_nan(mk, wr[k][i]);
         bm[k] = mk;
-        m = umaxmag2(m, mk);
+        m = maxabs2_nan(m, mk);
       }
     }
     for (int b = threadIdx.x + kActRegBlocks * kActThreads; b < nb; b += kActThreads) {
       const uint4 lo = ldg_stream(xr + b * 16);
       const uint4 hi = ldg_stream(xr + b * 16 + 8);
-      m = umaxmag2(m, lo.x); m = umaxmag2(m, lo.y); m = umaxmag2(m, lo.z); m = umaxmag2(m, lo.w);
-      m = umaxmag2(m, hi.x); m = umaxmag2(m, hi.y); m = umaxmag2(m, hi.z); m = umaxmag2(m, hi.w);
+      m = maxabs2_nan(m, maxabs2_nan(maxabs2_nan(lo.x, lo.y), maxabs2_nan(lo.z, lo.w)));
+      m = maxabs2_nan(m, maxabs2_nan(maxabs2_nan(hi.x, hi.y), maxabs2_nan(hi.z, hi.w)));
     }
+    m &= 0x7fff7fffu;  // magnitudes: NaN patterns order above infinity as integers
     uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
     mm = __reduce_max_sync(0xffffffffu, mm);
     if (lane == 0) red[warp] = mm;
@@ -891,12 +892,13 @@ __global__ void __launch_bounds__(kActWarpThreads)
     uint32_t m = 0;
 #pragma unroll
     for (int k = 0; k < kActWarpBlocks; k++) {
-      uint32_t mk = 0;
+      uint32_t mk = maxabs2_nan(wr[k][0], wr[k][1]);
 #pragma unroll
-      for (int i = 0; i < 8; i++) mk = umaxmag2(mk, wr[k][i]);
+      for (int i = 2; i < 8; i++) mk = maxabs2_nan(mk, wr[k][i]);
       bm[k] = mk;
-      m = umaxmag2(m, mk);
+      m = maxabs2_nan(m, mk);
     }
+    m &= 0x7fff7fffu;  // magnitudes: NaN patterns order above infinity as integers
     uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
     mm = __reduce_max_sync(0xffffffffu, mm);
     const float am = __uint_as_float(mm);
@@ -996,18 +998,20 @@ __global__ void __launch_bounds__(kActStreamThreads, 1)
       }
       return;
     }
-    // row amax: magnitude maximum on bf16 bit patterns (exact; NaN above
-    // inf), four independent chains
+    // row amax: magnitude maximum of bf16 pairs (a selection, hence exact;
+    // a NaN propagates), four independent chains
     uint32_t m4[4] = {0, 0, 0, 0};
 #pragma unroll 4
     for (int c = lane; c < (int)(rowbytes >> 4); c += 32) {
       const uint4 v = *reinterpret_cast<const uint4*>(buf + c * 16);
-      m4[0] = umaxmag2(m4[0], v.x);
-      m4[1] = umaxmag2(m4[1], v.y);
-      m4[2] = umaxmag2(m4[2], v.z);
-      m4[3] = umaxmag2(m4[3], v.w);
+      m4[0] = maxabs2_nan(m4[0], v.x);
+      m4[1] = maxabs2_nan(m4[1], v.y);
+      m4[2] = maxabs2_nan(m4[2], v.z);
+      m4[3] = maxabs2_nan(m4[3], v.w);
     }
-    const uint32_t m = umaxmag2(umaxmag2(m4[0], m4[1]), umaxmag2(m4[2], m4[3]));
+    // magnitudes: NaN patterns order above infinity as integers
+    const uint32_t m =
+        maxabs2_nan(maxabs2_nan(m4[0], m4[1]), maxabs2_nan(m4[2], m4[3])) & 0x7fff7fffu;
     uint32_t mm = max(m & 0xffffu, m >> 16) << 16;
     mm = __reduce_max_sync(0xffffffffu, mm);
     const float am = __uint_as_float(mm);
