@@ -1173,23 +1173,26 @@ cudaError_t launch_dequant(const uint8_t* codes, const uint8_t* scales, const fl
 }
 
 // ------------------------------------------------------- transposed dequant
-// Tiles of 128 out-rows x 256 in-columns of the rowwise copy.  Thread
-// (g = tid & 15, b = tid >> 4) dequantises out-rows 8g .. 8g+7 of 16-wide
-// block column b and writes each of its 16 in-columns straight to global
-// memory as one 16-byte run of an output row: the 16 lanes of a warp that
-// share a block column write 16 x 16 contiguous bytes of one row of the
-// [nexp, in, out] result, so a warp store is two full 256-byte runs and no
-// shared staging, fence, barrier or TMA store is needed.  Consecutive tiles
-// step along `out` first, so the CTAs running together fill neighbouring
-// pieces of the same output rows.  Measured alternatives: staging the tile
-// in shared memory and storing it with TMA boxes was the same speed (2 %
-// slower on the down stack); taller tiles (256 or 512 out-rows, longer
-// contiguous output per row) and one block column per warp (512-byte
-// stores) were 15-35 % slower, as were three or four CTAs per SM: the
-// row-strided code loads rely on L1 keeping the 32-byte sectors that the
-// neighbouring warp also reads.
+// Tiles of 128 out-rows x 256 NB in-columns of the rowwise copy.  Thread
+// (g = tid & 15, b = tid >> 4) dequantises out-rows 8g .. 8g+7 of the NB
+// 16-wide block columns NB b .. NB b + NB - 1 and writes each of its 16 NB
+// in-columns straight to global memory as one 16-byte run of an output row:
+// the 16 lanes of a warp that share b write 16 x 16 contiguous bytes of one
+// row, so a warp store is two full 256-byte runs and no shared staging,
+// fence, barrier or TMA store is needed.  Consecutive tiles step along `out`
+// first, so the CTAs running together fill neighbouring pieces of the same
+// output rows.  NB = 2 when `in` is a multiple of 32: a warp's code load then
+// takes 32 contiguous bytes of each of 16 rows (whole sectors when the rows
+// are 32-byte aligned) and each thread has twice the bytes in flight; with
+// NB = 1 a warp takes 16 bytes of each row and the neighbouring warp the
+// other half of the sector.  Measured alternatives: staging the tile in
+// shared memory and storing it with TMA boxes was the same speed (2 % slower
+// on the down stack); taller tiles (256 or 512 out-rows, longer contiguous
+// output per row) and one block column per warp (512-byte stores) were
+// 15-35 % slower, as were three or four CTAs per SM.
 constexpr int kTqThreads = 256;
 
+template <int NB>
 __global__ void __launch_bounds__(kTqThreads, 2)
     k_dequant_t(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                 const float* __restrict__ G, int out, int in, FastDiv per_exp, FastDiv by_tiles_r,
@@ -1197,6 +1200,7 @@ __global__ void __launch_bounds__(kTqThreads, 2)
   __shared__ ScaleEnt tbl[128];
   build_scale_table(tbl);
   __syncthreads();
+  constexpr int kTC = 256 * NB;  // in-columns per tile
   const int tid = threadIdx.x;
   const int g = tid & 15, b = tid >> 4;
   const int64_t in_h = in >> 1, in_16 = in >> 4;
@@ -1204,40 +1208,52 @@ __global__ void __launch_bounds__(kTqThreads, 2)
     const uint32_t e = per_exp.div(t);
     const uint32_t rem = t - e * per_exp.d;
     const int tc = (int)by_tiles_r.div(rem), tr = (int)(rem - tc * by_tiles_r.d);
-    const int r0 = tr * 128, c0 = tc * 256;
-    if (g * 8 >= min(128, out - r0) || b * 16 >= min(256, in - c0)) continue;
+    const int r0 = tr * 128, c0 = tc * kTC;
+    if (g * 8 >= min(128, out - r0) || b * 16 * NB >= min(kTC, in - c0)) continue;
     const int64_t grow = (int64_t)e * out + r0 + g * 8;
-    const uint8_t* pc = codes + grow * in_h + (c0 >> 1) + b * 8;
-    const uint8_t* ps = scales + grow * in_16 + (c0 >> 4) + b;
-    uint2 cw[8];
-    uint32_t S2[8];
+    const uint8_t* pc = codes + grow * in_h + (c0 >> 1) + b * 8 * NB;
+    const uint8_t* ps = scales + grow * in_16 + (c0 >> 4) + b * NB;
+    // code words of out-row i: cw[i][2h], cw[i][2h + 1] hold block column h;
+    // sc[i] the row's NB scale bytes (block column h in byte h)
+    uint32_t cw[8][2 * NB], sc[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-      cw[i] = __ldg(reinterpret_cast<const uint2*>(pc + i * in_h));
-      S2[i] = __ldg(ps + i * in_16);
+      if constexpr (NB == 2) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(pc + i * in_h));
+        cw[i][0] = v.x; cw[i][1] = v.y; cw[i][2] = v.z; cw[i][3] = v.w;
+        sc[i] = __ldg(reinterpret_cast<const uint16_t*>(ps + i * in_16));
+      } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(pc + i * in_h));
+        cw[i][0] = v.x; cw[i][1] = v.y;
+        sc[i] = __ldg(ps + i * in_16);
+      }
     }
-#pragma unroll
-    for (int i = 0; i < 8; i++) S2[i] = pos_s2(tbl[S2[i] & 0x7f]);
     const float Gv = G[e];
     const float2 G2 = make_float2(Gv, Gv);
-    // output row (in-index) c0 + 16b + j, out-columns r0 + 8g .. +7
-    uint16_t* const d0 = dst + ((int64_t)e * in + c0 + 16 * b) * out + r0 + 8 * g;
 #pragma unroll
-    for (int J = 0; J < 8; J++) {
-      uint32_t v[8];  // bf16 pair (in-columns 2J, 2J+1) of out-row i
+    for (int h = 0; h < NB; h++) {
+      uint32_t S2[8];
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const uint32_t word = J < 4 ? cw[i].x : cw[i].y;
-        const uint32_t h = e2m1x2_dec(__byte_perm(word, 0, 0x4440 + (J & 3)));
-        const float2 y = __fmul2_rn(cs_exact(h, S2[i]), G2);
-        v[i] = bf16x2_rn(y.x, y.y);
+      for (int i = 0; i < 8; i++) S2[i] = pos_s2(tbl[(sc[i] >> (8 * h)) & 0x7f]);
+      // output row (in-index) c0 + 16 (NB b + h) + j, out-columns r0 + 8g .. +7
+      uint16_t* const d0 = dst + ((int64_t)e * in + c0 + 16 * (NB * b + h)) * out + r0 + 8 * g;
+#pragma unroll
+      for (int J = 0; J < 8; J++) {
+        uint32_t v[8];  // bf16 pair (in-columns 2J, 2J+1) of out-row i
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          const uint32_t word = cw[i][2 * h + (J >> 2)];
+          const uint32_t hh = e2m1x2_dec(__byte_perm(word, 0, 0x4440 + (J & 3)));
+          const float2 y = __fmul2_rn(cs_exact(hh, S2[i]), G2);
+          v[i] = bf16x2_rn(y.x, y.y);
+        }
+        stg_stream(d0 + (int64_t)(2 * J) * out,
+                   make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                              __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410)));
+        stg_stream(d0 + (int64_t)(2 * J + 1) * out,
+                   make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632),
+                              __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632)));
       }
-      stg_stream(d0 + (int64_t)(2 * J) * out,
-                 make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
-                            __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410)));
-      stg_stream(d0 + (int64_t)(2 * J + 1) * out,
-                 make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632),
-                            __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632)));
     }
   }
 }
@@ -1245,7 +1261,11 @@ __global__ void __launch_bounds__(kTqThreads, 2)
 cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const float* G,
                              int64_t nexp, int out, int in, uint16_t* dst, cudaStream_t s) {
   const DevInfo* di = device_info();
-  const int tiles_r = (out + 127) / 128, tiles_c = (in + 255) / 256;
+  // two block columns per thread when every row holds an even number of
+  // blocks (its codes then start on a 16-byte boundary, its scales on a
+  // 2-byte one)
+  const bool two = (in % 32) == 0;
+  const int tiles_r = (out + 127) / 128, tiles_c = two ? (in + 511) / 512 : (in + 255) / 256;
   const int64_t ntiles = nexp * tiles_r * tiles_c;
   if (ntiles == 0) return cudaSuccess;
   if (ntiles >= (1ll << 31) - (1ll << 24)) return cudaErrorInvalidValue;
@@ -1255,7 +1275,12 @@ cudaError_t launch_dequant_t(const uint8_t* codes, const uint8_t* scales, const 
   br.d = (uint32_t)tiles_r;
   make_fastdiv(br.d, &br.m, &br.s);
   const int grid = (int)std::min<int64_t>(ntiles, (int64_t)di->sms * 2);
-  k_dequant_t<<<grid, kTqThreads, 0, s>>>(codes, scales, G, out, in, pe, br, (uint32_t)ntiles, dst);
+  if (two)
+    k_dequant_t<2><<<grid, kTqThreads, 0, s>>>(codes, scales, G, out, in, pe, br,
+                                                (uint32_t)ntiles, dst);
+  else
+    k_dequant_t<1><<<grid, kTqThreads, 0, s>>>(codes, scales, G, out, in, pe, br,
+                                                (uint32_t)ntiles, dst);
   return cudaGetLastError();
 }
 
