@@ -87,18 +87,13 @@ __global__ void __launch_bounds__(kNqThreads)
   const int64_t stride = (int64_t)gridDim.x * kNqThreads;
   const float2 k16 = make_float2(16.0f, 16.0f), k96 = make_float2(96.0f, 96.0f);
   const bool w32 = (reinterpret_cast<uintptr_t>(w) & 31) == 0;
-  // The loop bound is taken at the warp's first lane so that whole warps
-  // stay together for the shuffle; lanes past the end only skip the stores.
-  for (int64_t h = (int64_t)blockIdx.x * kNqThreads + threadIdx.x; h - (threadIdx.x & 31) < nhalf;
-       h += stride) {
-    const bool act = h < nhalf;
-    // the half block's 64 bytes as two 32-byte loads (one full sector each)
-    // when the stack is 32-byte aligned, else as four 16-byte loads
-    uint4 v[4];
-    if (act && !w32) {
+  // half block h's 64 bytes as two 32-byte loads (one full sector each) when
+  // the stack is 32-byte aligned, else as four 16-byte loads; zeros past the end
+  auto load = [&](int64_t h, uint4 v[4]) {
+    if (h < nhalf && !w32) {
 #pragma unroll
       for (int u = 0; u < 4; u++) v[u] = __ldg(reinterpret_cast<const uint4*>(w + h * 32 + u * 8));
-    } else if (act) {
+    } else if (h < nhalf) {
       uint32_t a[8], b[8];
       ldg32(w + h * 32, a);
       ldg32(w + h * 32 + 16, b);
@@ -110,6 +105,17 @@ __global__ void __launch_bounds__(kNqThreads)
 #pragma unroll
       for (int u = 0; u < 4; u++) v[u] = make_uint4(0, 0, 0, 0);
     }
+  };
+  // The loop bound is taken at the warp's first lane so that whole warps
+  // stay together for the shuffle; lanes past the end only skip the stores.
+  // Each thread loads its next half block before it quantises this one, so
+  // two are in flight per thread.
+  int64_t h = (int64_t)blockIdx.x * kNqThreads + threadIdx.x;
+  uint4 v[4], vn[4];
+  load(h, v);
+  for (; h - (threadIdx.x & 31) < nhalf; h += stride) {
+    const bool act = h < nhalf;
+    load(h + stride, vn);
     uint32_t m = maxabs2_nan(v[0].x, v[0].y);
     m = maxabs2_nan(m, v[0].z);
     m = maxabs2_nan(m, v[0].w);
@@ -149,6 +155,8 @@ __global__ void __launch_bounds__(kNqThreads)
         if (status && !isfinite(am)) atomicOr(status, kStatusNonFinite);
       }
     }
+#pragma unroll
+    for (int u = 0; u < 4; u++) v[u] = vn[u];
   }
 }
 
